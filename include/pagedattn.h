@@ -1,0 +1,189 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 (sm_103a) paged-KV attention library.
+ *
+ * The calls follow the hot path described on the AstrAI commit pages:
+ *   - commit 398e8a3 (tests/inference/test_cache.py): inference on packed 3-D
+ *     [tokens, heads, head_dim] tensors; rotary embedding on packed inputs;
+ *     int32 page-table, request-row and cache-location indices; K/V stored at
+ *     buffer[layer_id, loc] of per-layer [n_layers, size, n_kv_heads, head_dim]
+ *     buffers; split-KV decode into workspace-owned partials (decode_o_part,
+ *     decode_ml_part) pre-allocated once, zero allocation in the decode loop, so
+ *     every address is stable under CUDA-graph capture;
+ *   - commit e58a728 (docs/developer/architecture.md): rotary from a real cos/sin
+ *     table; prompts packed into one forward and addressed by cumulative query
+ *     lengths (qo_indptr); paged prefill (attn_paged_prefill); decode reading
+ *     K/V through req_to_token.
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *     row-major, with 16-byte aligned base addresses.  bf16 data travel as
+ *     IEEE bfloat16 (2 bytes), indices as int32, tables and workspaces as fp32.
+ *   - The library allocates nothing, keeps no per-call state and never
+ *     synchronises the stream (pa_get_error excepted).  Work is enqueued on the
+ *     given stream; every call except pa_get_error can be captured in a CUDA
+ *     graph, since grid shapes depend only on call arguments and workspace
+ *     capacity, never on device-resident lengths.
+ *   - Validation first: every host-side check runs before any launch, and a
+ *     call that returns an error has enqueued nothing and written nothing.
+ *   - Device-side index errors (a cache slot, request row or position out of
+ *     range) never trap: the offending element is skipped (treated as masked,
+ *     or left unwritten) and a sticky bit is OR-ed into a device error word,
+ *     read outside the hot loop with pa_get_error.
+ *   - Return values are pa_status codes; PA_ERR_CUDA means a launch failed
+ *     (cudaGetLastError after the launch).
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_NULL = 1,         /* a required pointer is NULL */
+    PA_ERR_SHAPE = 2,        /* a size, count or index argument is out of range */
+    PA_ERR_ALIGN = 3,        /* a pointer is not 16-byte (workspace: 256-byte) aligned */
+    PA_ERR_UNSUPPORTED = 4,  /* head_dim / GQA group not supported by the kernels */
+    PA_ERR_WORKSPACE = 5,    /* workspace too small for this call */
+    PA_ERR_CUDA = 6,         /* a CUDA runtime / driver call failed */
+    PA_ERR_DEVICE_INDEX = 7  /* (pa_get_error only) the device error word is non-zero */
+} pa_status;
+
+/* Bits of the device error word. */
+#define PA_DEVERR_SLOT 0x1      /* a cache slot (loc or req_to_token entry) outside [0, size) */
+#define PA_DEVERR_ROW 0x2       /* a req_pool_indices entry outside [0, req_rows) */
+#define PA_DEVERR_LEN 0x4       /* a seq_len / indptr length outside [0, max_ctx] or n_r > L_r */
+#define PA_DEVERR_POS 0x8       /* a rotary position outside [0, max_pos) */
+
+/* Shape of one of the two KV buffers, bf16 [n_layers, size, n_kv_heads, head_dim];
+ * slot `loc` of layer `l` starts at element ((l * size + loc) * n_kv_heads) * head_dim. */
+typedef struct {
+    int n_layers;
+    int size;        /* slots per layer */
+    int n_kv_heads;
+    int head_dim;
+} pa_kv_shape;
+
+/* Human-readable name of a status code (static string). */
+const char *pa_status_string(pa_status s);
+
+/* ----------------------------------------------------------- workspaces
+ * A workspace is one caller-allocated device buffer, 256-byte aligned.  Its
+ * first 4 bytes are the device error word.  Initialise it once with
+ * pa_workspace_init before first use (it zeroes the error word and the decode
+ * merge counters, which the decode kernel afterwards keeps at zero itself).
+ *
+ * Decode layout, derived only from (workspace_bytes, n_q_heads, n_kv_heads,
+ * head_dim, max_splits), so changing the batch between calls moves nothing:
+ *   [0, 256)   error word + padding
+ *   counters   int32 [cap_batch * n_kv_heads]  (one per request x kv head)
+ *   ml_part    fp32  [max_splits, cap_batch, n_q_heads, 2]   (running max in
+ *              log2 units, running sum) -- the pages' decode_ml_part
+ *   o_part     fp32  [max_splits, cap_batch, n_q_heads, head_dim]  unnormalised
+ *              partial outputs -- the pages' decode_o_part
+ * where cap_batch is the largest batch the bytes hold. */
+size_t pa_decode_workspace_bytes(int max_batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int max_splits);
+
+/* Prefill workspace: the error word plus a small fixed area. */
+size_t pa_prefill_workspace_bytes(void);
+
+/* Zero the whole workspace on `st` (cudaMemsetAsync).  Call once after
+ * allocation, outside any graph capture that replays it while work is in flight. */
+pa_status pa_workspace_init(void *workspace, size_t workspace_bytes, cudaStream_t st);
+
+/* Copy the workspace's device error word to *device_error.  Synchronises `st`
+ * (keep it out of the hot loop and out of graph capture).  Returns
+ * PA_ERR_DEVICE_INDEX if the word is non-zero, PA_OK otherwise.  The word is
+ * sticky: pa_workspace_init clears it. */
+pa_status pa_get_error(const void *workspace, int32_t *device_error, cudaStream_t st);
+
+/* Same, for a bare int32 error word passed to pa_kv_store / pa_rope_packed. */
+pa_status pa_get_error_word(const int32_t *error_word, int32_t *device_error, cudaStream_t st);
+
+/* --------------------------------------------------------------- KV store
+ * Commit 398e8a3: new tokens' K/V written at buffer[layer_id, loc] with int32
+ * cache locations.  For every token t < n_tokens and kv head h:
+ *     k_buf[layer_id, loc[t], h, :] = k_new[t, h, :]
+ *     v_buf[layer_id, loc[t], h, :] = v_new[t, h, :]
+ * A bit-exact copy.  k_new / v_new: bf16 [n_tokens, n_kv_heads, head_dim];
+ * loc: int32 [n_tokens].  head_dim must be a multiple of 8.  Locations must be
+ * distinct within one call (duplicates race).  A location outside [0, size)
+ * is skipped and sets PA_DEVERR_SLOT in *error_word (if error_word != NULL).
+ * n_tokens == 0 is a no-op. */
+pa_status pa_kv_store(void *k_buf, void *v_buf, pa_kv_shape s, int layer_id, const void *k_new,
+                      const void *v_new, const int32_t *loc, int n_tokens, int32_t *error_word,
+                      cudaStream_t st);
+
+/* ----------------------------------------------------------------- RoPE
+ * Commit 398e8a3 (rotary extended to packed 3-D inputs) and commit e58a728
+ * (cos/sin table, not a complex buffer).  In place on q bf16
+ * [n_tokens, n_q_heads, head_dim] and k bf16 [n_tokens, n_kv_heads, head_dim]
+ * (k may be NULL when n_kv_heads == 0).  For token t with p = positions[t]
+ * and pair i < head_dim/2 (interleaved pairs (2i, 2i+1)):
+ *     x[2i]   <- x[2i] * cos_tab[p, i] - x[2i+1] * sin_tab[p, i]
+ *     x[2i+1] <- x[2i] * sin_tab[p, i] + x[2i+1] * cos_tab[p, i]
+ * in fp32, rounded to bf16 (nearest even).  cos_tab / sin_tab: fp32
+ * [max_pos, head_dim/2].  head_dim must be a multiple of 8.  A position outside
+ * [0, max_pos) leaves that token unchanged and sets PA_DEVERR_POS. */
+pa_status pa_rope_packed(void *q, int n_q_heads, void *k, int n_kv_heads, int head_dim,
+                         const int32_t *positions, int n_tokens, const float *cos_tab,
+                         const float *sin_tab, int max_pos, int32_t *error_word, cudaStream_t st);
+
+/* ------------------------------------------------------------ decode attn
+ * Commit 398e8a3: packed decode over the paged cache with int32 indices and
+ * split-KV partials in a caller workspace; commit e58a728: K/V read through
+ * req_to_token.  For request b < batch with n = seq_lens[b] and
+ * row = req_pool_indices[b], and query head hq with kv head h = hq / G
+ * (G = n_q_heads / n_kv_heads):
+ *     s_j   = scale * <q[b, hq, :], K[layer_id, req_to_token[row, j], h, :]>, j < n
+ *     out[b, hq, :] = sum_j softmax(s)_j * V[layer_id, req_to_token[row, j], h, :]
+ * q, out: bf16 [batch, n_q_heads, head_dim]; req_to_token: int32
+ * [req_rows, max_ctx]; req_pool_indices, seq_lens: int32 [batch] (device).
+ * seq_lens counts the current token, whose K/V must already be stored.
+ * n == 0 writes zeros.  Entries req_to_token[row, j >= n] are never read.
+ * Computed as split-KV flash-decoding: each (request, kv head) range is cut
+ * into at most max_splits pieces, chosen on the device from seq_lens and the
+ * SM count, whose fp32 partials (o_part, ml_part) are merged by log-sum-exp in
+ * a fixed order (run-to-run bit-identical).
+ * Supported: head_dim in {64, 128}; 1 <= G <= 16; batch <= 4096 and <= the
+ * workspace's cap_batch for these head counts and max_splits. */
+pa_status pa_paged_decode_attn(const void *q, int batch, int n_q_heads, const void *k_buf,
+                               const void *v_buf, pa_kv_shape s, int layer_id,
+                               const int32_t *req_to_token, int req_rows, int max_ctx,
+                               const int32_t *req_pool_indices, const int32_t *seq_lens,
+                               float scale, void *workspace, size_t workspace_bytes,
+                               int max_splits, void *out, cudaStream_t st);
+
+/* ----------------------------------------------------------- prefill attn
+ * Commit e58a728: packed prompts with a shared prefix start in one forward,
+ * paged prefill (attn_paged_prefill), rows located by cumulative query lengths;
+ * commit 398e8a3: request mappings for cached prefix pages.  Request r owns
+ * packed query rows qo_indptr[r] .. qo_indptr[r+1]-1 (n_r rows) and has
+ * L_r = kv_indptr[r+1] - kv_indptr[r] cached tokens (prefix p_r = L_r - n_r,
+ * then the n_r new tokens, whose K/V must already be stored).  Query i of
+ * request r (position p_r + i) attends to positions 0 .. p_r + i through
+ * req_to_token[req_pool_indices[r], position]:
+ *     out[t, hq, :] = sum_j softmax(scale * <q[t, hq], K_j>)_j V_j
+ * q, out: bf16 [n_tokens, n_q_heads, head_dim]; qo_indptr, kv_indptr: int32
+ * [n_reqs + 1] (device), qo_indptr[n_reqs] == n_tokens.  QK^T and PV run on
+ * tcgen05 tensor cores (bf16 operands, fp32 accumulation in tensor memory, P
+ * rounded to bf16).  Supported: head_dim 128; G in {1, 2, 4, 8, 16}.
+ * n_r > L_r or L_r > max_ctx sets PA_DEVERR_LEN and skips that request. */
+pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_heads, const void *k_buf,
+                                const void *v_buf, pa_kv_shape s, int layer_id,
+                                const int32_t *qo_indptr, const int32_t *kv_indptr, int n_reqs,
+                                const int32_t *req_to_token, int req_rows, int max_ctx,
+                                const int32_t *req_pool_indices, float scale, void *workspace,
+                                size_t workspace_bytes, void *out, cudaStream_t st);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

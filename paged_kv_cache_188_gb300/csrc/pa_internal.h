@@ -1,0 +1,31 @@
+// pa_internal.h -- host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+constexpr int kWorkspaceHeader = 256;   // error word + padding at the start of a workspace
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+// SM count of the current device (cached per device; a property, not call state).
+int num_sms();
+
+// Decode workspace geometry, a pure function of its arguments.
+struct DecodeWsLayout {
+    int cap_batch;
+    size_t counters_off, ml_off, o_off, total;
+};
+DecodeWsLayout decode_ws_layout(size_t workspace_bytes, int n_q_heads, int n_kv_heads, int head_dim,
+                                int max_splits);
+
+}  // namespace pa

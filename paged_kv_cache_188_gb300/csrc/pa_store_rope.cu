@@ -1,0 +1,133 @@
+// pa_store_rope.cu -- the two bandwidth-bound elementwise steps of the path:
+//   pa_kv_store    : new tokens' K/V written at buffer[layer_id, loc]
+//                    (AstrAI commit 398e8a3, tests/inference/test_cache.py:
+//                    single advanced indexing buffer[layer_id, loc], int32 loc)
+//   pa_rope_packed : rotary embedding on packed [T, H, D] q and k from a cos/sin
+//                    table (commit 398e8a3: rotary extended to packed 3-D
+//                    inputs; commit e58a728, docs/developer/architecture.md:
+//                    a real cos/sin freqs_cis table)
+// Both move 16-byte vectors: one thread per 16 bytes of a row, rows contiguous
+// in memory, so every warp touches whole 128-byte lines.
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// One thread copies one 16-byte chunk of one token's K row and the same chunk
+// of its V row.  row_chunks = Hkv * D / 8 chunks per token.
+__global__ void __launch_bounds__(256) kv_store_kernel(uint4 *__restrict__ k_layer, uint4 *__restrict__ v_layer,
+                                                       const uint4 *__restrict__ k_new,
+                                                       const uint4 *__restrict__ v_new,
+                                                       const int32_t *__restrict__ loc, int64_t n_chunks,
+                                                       int row_chunks, int size, int32_t *err)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_chunks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / row_chunks;
+        const int c = (int)(i - t * row_chunks);
+        const int32_t slot = __ldg(loc + t);
+        if (slot < 0 || slot >= size) {
+            if (c == 0) set_error(err, PA_DEVERR_SLOT);
+            continue;
+        }
+        const uint4 kv = __ldcs(k_new + i);
+        const uint4 vv = __ldcs(v_new + i);
+        const int64_t dst = (int64_t)slot * row_chunks + c;
+        k_layer[dst] = kv;
+        v_layer[dst] = vv;
+    }
+}
+
+// One thread rotates 8 consecutive elements (4 interleaved pairs) of one head
+// vector.  Heads [0, Hq) index q, heads [Hq, Hq + Hkv) index k.
+__global__ void __launch_bounds__(256) rope_kernel(uint4 *__restrict__ q, uint4 *__restrict__ k, int Hq, int Hkv,
+                                                   int head_chunks, const int32_t *__restrict__ positions,
+                                                   int64_t n_chunks, const float4 *__restrict__ cos_tab,
+                                                   const float4 *__restrict__ sin_tab, int max_pos,
+                                                   int32_t *err)
+{
+    const int heads = Hq + Hkv;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_chunks;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t th = i / head_chunks;     // token * heads + head
+        const int c = (int)(i - th * head_chunks);
+        const int64_t t = th / heads;
+        const int h = (int)(th - t * heads);
+        const int32_t p = __ldg(positions + t);
+        if (p < 0 || p >= max_pos) {
+            if (h == 0 && c == 0) set_error(err, PA_DEVERR_POS);
+            continue;
+        }
+        uint4 *ptr = h < Hq ? q + (t * Hq + h) * head_chunks + c : k + (t * Hkv + (h - Hq)) * head_chunks + c;
+        // pairs 4c .. 4c+3 of this head: table row p, columns 4c .. 4c+3
+        const float4 cs = __ldg(cos_tab + (int64_t)p * head_chunks + c);
+        const float4 sn = __ldg(sin_tab + (int64_t)p * head_chunks + c);
+        uint4 x = *ptr;
+        const float cc[4] = {cs.x, cs.y, cs.z, cs.w};
+        const float ss[4] = {sn.x, sn.y, sn.z, sn.w};
+        uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162 *>(&w[j]);
+            const float x0 = __low2float(pr), x1 = __high2float(pr);
+            const float y0 = fmaf(x0, cc[j], -x1 * ss[j]);
+            const float y1 = fmaf(x0, ss[j], x1 * cc[j]);
+            w[j] = pack_bf16x2(y0, y1);
+        }
+        *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+static int grid_for(int64_t n_threads, int block)
+{
+    int64_t g = (n_threads + block - 1) / block;
+    const int cap = num_sms() * 16;
+    return (int)(g < cap ? (g > 0 ? g : 1) : cap);
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status pa_kv_store(void *k_buf, void *v_buf, pa_kv_shape s, int layer_id, const void *k_new,
+                                 const void *v_new, const int32_t *loc, int n_tokens, int32_t *error_word,
+                                 cudaStream_t st)
+{
+    if (n_tokens < 0 || s.n_layers <= 0 || s.size <= 0 || s.n_kv_heads <= 0 || s.head_dim <= 0)
+        return PA_ERR_SHAPE;
+    if (layer_id < 0 || layer_id >= s.n_layers) return PA_ERR_SHAPE;
+    if (s.head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+    if (n_tokens == 0) return PA_OK;
+    if (!k_buf || !v_buf || !k_new || !v_new || !loc) return PA_ERR_NULL;
+    if (!aligned16(k_buf) || !aligned16(v_buf) || !aligned16(k_new) || !aligned16(v_new) || !aligned4(loc))
+        return PA_ERR_ALIGN;
+    if (error_word && !aligned4(error_word)) return PA_ERR_ALIGN;
+    const int row_chunks = s.n_kv_heads * s.head_dim / 8;
+    const int64_t layer_off = (int64_t)layer_id * s.size * row_chunks;
+    const int64_t n_chunks = (int64_t)n_tokens * row_chunks;
+    kv_store_kernel<<<grid_for(n_chunks, 256), 256, 0, st>>>(
+        static_cast<uint4 *>(k_buf) + layer_off, static_cast<uint4 *>(v_buf) + layer_off,
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), loc, n_chunks, row_chunks, s.size,
+        error_word);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_rope_packed(void *q, int n_q_heads, void *k, int n_kv_heads, int head_dim,
+                                    const int32_t *positions, int n_tokens, const float *cos_tab,
+                                    const float *sin_tab, int max_pos, int32_t *error_word, cudaStream_t st)
+{
+    if (n_tokens < 0 || n_q_heads < 0 || n_kv_heads < 0 || head_dim <= 0 || max_pos <= 0) return PA_ERR_SHAPE;
+    if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+    if (n_tokens == 0 || n_q_heads + n_kv_heads == 0) return PA_OK;
+    if ((n_q_heads > 0 && !q) || (n_kv_heads > 0 && !k) || !positions || !cos_tab || !sin_tab) return PA_ERR_NULL;
+    if ((q && !aligned16(q)) || (k && !aligned16(k)) || !aligned4(positions) || !aligned16(cos_tab) ||
+        !aligned16(sin_tab))
+        return PA_ERR_ALIGN;
+    if (error_word && !aligned4(error_word)) return PA_ERR_ALIGN;
+    const int head_chunks = head_dim / 8;
+    const int64_t n_chunks = (int64_t)n_tokens * (n_q_heads + n_kv_heads) * head_chunks;
+    rope_kernel<<<grid_for(n_chunks, 256), 256, 0, st>>>(
+        static_cast<uint4 *>(q), static_cast<uint4 *>(k), n_q_heads, n_kv_heads, head_chunks, positions, n_chunks,
+        reinterpret_cast<const float4 *>(cos_tab), reinterpret_cast<const float4 *>(sin_tab), max_pos, error_word);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

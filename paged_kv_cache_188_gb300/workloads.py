@@ -77,8 +77,9 @@ def _assign_slots(lens, page_size, n_pages, gen, shared_prefix=None):
     """Per request, the slot of every logical token, page-granular.
 
     ``shared_prefix``: optional (group_size, prefix_len); requests of one group
-    map their first min(len, prefix_len) tokens onto the group's common pages
-    (radix-style prefix reuse), the rest onto private pages."""
+    map their first tokens, up to prefix_len, onto the group's common pages
+    (radix-style prefix reuse), the rest onto private pages.  The page that
+    holds a request's last token is always private."""
     perm = torch.randperm(n_pages, generator=gen)
     nxt = 0
 
@@ -101,7 +102,9 @@ def _assign_slots(lens, page_size, n_pages, gen, shared_prefix=None):
             g = b // gsz
             if g not in group_pages:
                 group_pages[g] = take(plen // page_size)
-            k_shared = min(n_req_pages, plen // page_size)
+            # the page holding the request's newest token stays private: a
+            # request never writes into pages it shares with others
+            k_shared = min(max(n - 1, 0) // page_size, plen // page_size)
             pages = torch.cat([group_pages[g][:k_shared], take(n_req_pages - k_shared)])
         else:
             pages = take(n_req_pages)

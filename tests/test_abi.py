@@ -1,0 +1,107 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol the header
+declares, sizes workspaces consistently, and rejects bad arguments on the host
+before any launch (these calls return before touching the CUDA runtime)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_188_gb300 import api
+from paged_kv_cache_188_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return api.lib()
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "pagedattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = header_symbols()
+    assert "pa_paged_decode_attn" in syms and "pa_paged_prefill_attn" in syms
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(api.EXPORTS) == set(syms)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.pa_status_string(code).decode().startswith(api.STATUS[code])
+
+
+def test_decode_workspace_size_monotone_and_sufficient(lib):
+    small = api.pa_decode_workspace_bytes(1, 32, 8, 128, 64)
+    big = api.pa_decode_workspace_bytes(256, 64, 8, 128, 64)
+    assert 0 < small < big
+    # o_part + ml_part + counters for 256 requests at least
+    assert big >= 256 * 64 * 64 * 128 * 4
+    assert api.pa_decode_workspace_bytes(0, 32, 8, 128, 0) == 0
+    assert api.pa_prefill_workspace_bytes() >= 256
+
+
+FAKE = 0x10000000  # a 256-byte aligned non-null address; the calls below fail before using it
+
+
+def _shape(n_layers=2, size=64, hkv=2, d=64):
+    return api.KvShape(n_layers, size, hkv, d)
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, batch=1, hq=8, k=FAKE, v=FAKE, s=_shape(), layer=0, r2t=FAKE, rows=1, max_ctx=16,
+             rpi=FAKE, sl=FAKE, scale=0.125, ws=FAKE, ws_bytes=api.pa_decode_workspace_bytes(1, 8, 2, 64, 4),
+             splits=4, out=FAKE)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.pa_paged_decode_attn(P(a["q"]), a["batch"], a["hq"], P(a["k"]), P(a["v"]), a["s"], a["layer"],
+                                    P(a["r2t"]), a["rows"], a["max_ctx"], P(a["rpi"]), P(a["sl"]), a["scale"],
+                                    P(a["ws"]), a["ws_bytes"], a["splits"], P(a["out"]), None)
+
+
+def test_decode_host_validation(lib):
+    assert _decode(lib, layer=2) == 2                        # layer out of range
+    assert _decode(lib, hq=7) == 2                           # Hq not a multiple of Hkv
+    assert _decode(lib, s=_shape(d=96)) == 4                 # unsupported head_dim
+    assert _decode(lib, hq=64) == 4                          # G = 32 > 16
+    assert _decode(lib, splits=0) == 2
+    assert _decode(lib, splits=257) == 2
+    assert _decode(lib, batch=4097) == 2
+    assert _decode(lib, ws=0) == 1
+    assert _decode(lib, ws=FAKE + 16) == 3                   # workspace must be 256-byte aligned
+    assert _decode(lib, ws_bytes=100) == 5
+    assert _decode(lib, batch=2) == 5                        # workspace sized for one request
+    assert _decode(lib, q=0) == 1
+    assert _decode(lib, q=FAKE + 2) == 3
+    assert _decode(lib, out=FAKE + 8) == 3
+    assert _decode(lib, sl=FAKE + 1) == 3
+    assert _decode(lib, batch=0, q=0, out=0) == 0            # empty batch: nothing to do
+
+
+def test_store_and_rope_host_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.pa_kv_store(P(FAKE), P(FAKE), _shape(), 2, P(FAKE), P(FAKE), P(FAKE), 4, None, None) == 2
+    assert lib.pa_kv_store(P(FAKE), P(FAKE), _shape(d=12), 0, P(FAKE), P(FAKE), P(FAKE), 4, None, None) == 4
+    assert lib.pa_kv_store(P(FAKE), None, _shape(), 0, P(FAKE), P(FAKE), P(FAKE), 4, None, None) == 1
+    assert lib.pa_kv_store(P(FAKE + 4), P(FAKE), _shape(), 0, P(FAKE), P(FAKE), P(FAKE), 4, None, None) == 3
+    assert lib.pa_kv_store(None, None, _shape(), 0, None, None, None, 0, None, None) == 0
+    assert lib.pa_rope_packed(P(FAKE), 4, P(FAKE), 2, 10, P(FAKE), 3, P(FAKE), P(FAKE), 16, None, None) == 4
+    assert lib.pa_rope_packed(P(FAKE), 4, None, 2, 64, P(FAKE), 3, P(FAKE), P(FAKE), 16, None, None) == 1
+    assert lib.pa_rope_packed(P(FAKE), 4, P(FAKE), 2, 64, P(FAKE), 3, P(FAKE + 4), P(FAKE), 16, None, None) == 3
+    assert lib.pa_rope_packed(P(FAKE), 4, P(FAKE), 2, 64, P(FAKE), -1, P(FAKE), P(FAKE), 16, None, None) == 2
+    assert lib.pa_workspace_init(None, 1024, None) == 1
+    assert lib.pa_workspace_init(P(FAKE + 8), 1024, None) == 3
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(api, "_lib", None)
+    monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        api.lib()
