@@ -1,0 +1,618 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV attention hot path on one GB300 (or N replicas).
+
+Headline workload: B=1 paged decode, Llama-style GQA (Hq=32, Hkv=8, D=128),
+KV buffers bf16 [32 layers, 65536 slots, 8, 128], page size 16 with randomly
+permuted pages, contexts {1K, 2K, 4K, 8K, 16K, 32K}.  One step is one decode
+step through all 32 layers at each of the six contexts; each layer-call runs
+the whole decode path through the C ABI:
+
+    pa_rope_packed (q, k of the new token) -> pa_kv_store (new K/V at its
+    slot) -> pa_paged_decode_attn (split-KV gather + LSE merge)
+
+i.e. 6 x 32 x 3 = 576 kernel launches per step, replayed as one CUDA graph.
+The 32-layer rotation gives every step an 8.5 GB footprint, far above the
+129 MB L2, so no flush is needed between steps.
+
+value  = algorithmic HBM bytes of the step / device time of the step (GB/s).
+e2e    = the same bytes / wall time of: pinned-host -> device copy of the
+         step's new-token inputs, the step, device -> pinned-host copy of the
+         step's attention outputs.
+roofline = the dominant kernel (decode attention) timed alone with CUDA events
+         on its stream, against the measured HBM copy bandwidth.
+
+Further lines of the same JSON object: the packed ragged prefill workload (16
+prompts, RoPE + KV store + causal paged prefill, TFLOP/s over unmasked
+pairs), the B=32 shared-prefix decode, the B=256 token-granular decode step.
+
+``--impl reference`` times the float64 CPU oracle on the same workload and
+metric (bounded sample per step).  N>1 (torchrun): independent replicas, one
+per GPU, each with its own cache; no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_188_gb300 import workloads as W  # noqa: E402
+
+SWEEP = [1024, 2048, 4096, 8192, 16384, 32768]
+N_LAYERS, SIZE, HQ, HKV, D, PAGE = 32, 65536, 32, 8, 128, 16
+MAX_SPLITS = 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
+# ncu capture, valid only while the kernel source is unchanged (sha256 prefix).
+NCU_TRAFFIC = {}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--only-main", action="store_true", help="skip the secondary workloads")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--profile", choices=["decode", "prefill", "rope", "store"], default=None,
+                   help="run a small fixed case of one kernel (for ncu captures) and exit")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        raw = json.load(open(path))
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+    def find(keys):
+        for k in keys:
+            if k in raw and isinstance(raw[k], (int, float)):
+                return float(raw[k])
+        for v in raw.values():
+            if isinstance(v, dict):
+                for k in keys:
+                    if k in v and isinstance(v[k], (int, float)):
+                        return float(v[k])
+        return None
+    peaks = {"hbm_gbs": find(["hbm_gbs"]), "bf16_tflops": find(["bf16_tflops"]),
+             "bf16_tflops_sustained": find(["bf16_tflops_sustained"])}
+    for k, v in FALLBACK_PEAKS.items():
+        if peaks[k] is None:
+            return dict(FALLBACK_PEAKS), "fallback"
+    return peaks, "measured"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], 0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_graph(graph, reps, stream):
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / reps   # ms per replay
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def src_sha(name):
+    path = os.path.join(ROOT, "paged_kv_cache_188_gb300", "csrc", name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+# ----------------------------------------------------------- byte counting
+
+def decode_bytes(n, Hq=HQ, Hkv=HKV, Dh=D):
+    """Algorithmic bytes of one decode call for one request of n tokens:
+    K+V rows, req_to_token entries, q in, out back, request metadata."""
+    return n * Hkv * Dh * 2 * 2 + n * 4 + Hq * Dh * 2 * 2 + 8
+
+
+def rope_bytes(T, Hq=HQ, Hkv=HKV, Dh=D):
+    return T * (Hq + Hkv) * Dh * 2 * 2 + T * (Dh // 2) * 4 * 2 + T * 4
+
+
+def store_bytes(T, Hkv=HKV, Dh=D):
+    return T * Hkv * Dh * 2 * 2 * 2 + T * 4
+
+
+# ------------------------------------------------------- headline workload
+
+class DecodeSweep:
+    """The 32-layer B=1 decode sweep, with every input resident on the device."""
+
+    def __init__(self, dev):
+        from paged_kv_cache_188_gb300 import api
+        self.api = api
+        self.dev = dev
+        kv = W.make_paged_kv(lens=[SWEEP[-1]], n_layers=N_LAYERS, size=SIZE, n_kv_heads=HKV, head_dim=D,
+                             page_size=PAGE, seed=2, max_ctx=SWEEP[-1], device=dev)
+        self.kv = kv
+        g = W.generator(2 + 104729, dev)
+        P, L = len(SWEEP), N_LAYERS
+        self.q = W.bf16_normal((P, L, 1, HQ, D), g, dev)
+        self.k_new = W.bf16_normal((P, L, 1, HKV, D), g, dev)
+        self.v_new = W.bf16_normal((P, L, 1, HKV, D), g, dev)
+        self.out = torch.zeros((P, L, 1, HQ, D), dtype=torch.bfloat16, device=dev)
+        cos, sin = W.rope_tables(W.ROPE_MAX_POS, D)
+        self.cos, self.sin = cos.to(dev), sin.to(dev)
+        row = int(kv.req_pool_indices[0])
+        self.seq = [torch.tensor([n], dtype=torch.int32, device=dev) for n in SWEEP]
+        self.pos = [torch.tensor([n - 1], dtype=torch.int32, device=dev) for n in SWEEP]
+        self.loc = [kv.req_to_token[row, n - 1:n].clone() for n in SWEEP]
+        self.ws = api.alloc_workspace(api.pa_decode_workspace_bytes(1, HQ, HKV, D, MAX_SPLITS), dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.scale = 1.0 / math.sqrt(D)
+        self.stream = torch.cuda.Stream(dev)
+        self.stream.wait_stream(torch.cuda.current_stream(dev))
+
+    def layer_call(self, p, l, what=("rope", "store", "decode")):
+        a, kv, s = self.api, self.kv, self.stream
+        if "rope" in what:
+            a.pa_rope_packed(self.q[p, l], self.k_new[p, l], self.pos[p], self.cos, self.sin, self.err, stream=s)
+        if "store" in what:
+            a.pa_kv_store(kv.k_buf, kv.v_buf, l, self.k_new[p, l], self.v_new[p, l], self.loc[p], self.err, stream=s)
+        if "decode" in what:
+            a.pa_paged_decode_attn(self.q[p, l], kv.k_buf, kv.v_buf, l, kv.req_to_token, kv.req_pool_indices,
+                                   self.seq[p], self.scale, self.ws, MAX_SPLITS, self.out[p, l], stream=s)
+
+    def step(self, what=("rope", "store", "decode"), points=None):
+        for p in (range(len(SWEEP)) if points is None else points):
+            for l in range(N_LAYERS):
+                self.layer_call(p, l, what)
+
+    def step_bytes(self):
+        per_layer = [decode_bytes(n) + rope_bytes(1) + store_bytes(1) for n in SWEEP]
+        return N_LAYERS * sum(per_layer)
+
+    launches_per_step = 3 * N_LAYERS * len(SWEEP)
+
+
+def run_ours(args, rank, world, local):
+    from paged_kv_cache_188_gb300 import api, build
+    build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    sw = DecodeSweep(dev)
+    s = sw.stream
+    torch.cuda.set_stream(s)   # graph replays, events and copies all go to the launch stream
+    api.pa_workspace_init(sw.ws, stream=s)
+
+    # eager once, then capture the whole step as one graph
+    sw.step()
+    torch.cuda.synchronize()
+    g_step = capture(sw.step, s)
+    for _ in range(max(3, args.warmup)):
+        g_step.replay()
+    torch.cuda.synchronize()
+    step_bytes = sw.step_bytes()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record(s)
+        for _ in range(args.steps):
+            g_step.replay()
+        end.record(s)
+        end.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_step = max_over_ranks(start.elapsed_time(end) / args.steps, world)
+    total_bytes = sum_over_ranks(step_bytes, world)
+    value = total_bytes / (ms_step * 1e-3) / 1e9
+
+    # per-kernel device time: each kernel alone, captured per context, same data
+    per_point = []
+    dec_bytes_tot = dec_ms_tot = 0.0
+    reps = 20
+    for p, n in enumerate(SWEEP):
+        g = capture(lambda: sw.step(("decode",), [p]), s)
+        g.replay()
+        ms = time_graph(g, reps, s) / N_LAYERS
+        b = decode_bytes(n)
+        dec_bytes_tot += b
+        dec_ms_tot += ms
+        per_point.append({"seq_len": n, "us_per_layer": round(ms * 1e3, 3),
+                          "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                          "frac_of_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)})
+    g_rope = capture(lambda: sw.step(("rope",)), s)
+    g_store = capture(lambda: sw.step(("store",)), s)
+    n_calls = N_LAYERS * len(SWEEP)
+    rope_us = time_graph(g_rope, reps, s) / n_calls * 1e3
+    store_us = time_graph(g_store, reps, s) / n_calls * 1e3
+    dec_gbs = dec_bytes_tot / (dec_ms_tot * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC.get("decode")
+    traffic_val = None
+    if traffic and traffic.get("sha") == src_sha("pa_decode.cu"):
+        traffic_val = traffic.get("bytes_per_launch")
+
+    # end to end: pinned host inputs -> device, step, outputs -> pinned host
+    h_in = [t.cpu().pin_memory() for t in (sw.q, sw.k_new, sw.v_new)]
+    d_in = (sw.q, sw.k_new, sw.v_new)
+    h_out = torch.empty(sw.out.shape, dtype=sw.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(10, args.steps // 4)
+
+    def e2e_step():
+        with torch.cuda.stream(s):
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            g_step.replay()
+            h_out.copy_(sw.out, non_blocking=True)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world)
+    e2e_val = total_bytes / e2e_s / 1e9
+
+    dev_err = api.pa_get_error(sw.ws, stream=s) | api.pa_get_error_word(sw.err, stream=s)
+    line = {
+        "metric": "paged decode-attn HBM GB/s (% of peak) & us/layer; packed prefill TFLOP/s",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
+        "config": {"workload": "B=1 paged decode step (RoPE + KV store + split-KV decode), Hq=32 Hkv=8 D=128, "
+                               "KV [32 layers, 65536 slots, 8, 128] bf16, page 16, contexts 1K-32K x 32 layers",
+                   "contexts": SWEEP, "layers": N_LAYERS, "page_size": PAGE, "max_splits": MAX_SPLITS,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "no flush: 8.5 GB step footprint (32-layer rotation) >> 129 MB L2",
+                   "timing": "CUDA events on the launch stream around K replays of the captured step graph"},
+        "gpu_launches": sw.launches_per_step * args.steps,
+        "gpu_launches_per_step": sw.launches_per_step,
+        "frac_of_hbm_peak": round(value / peaks["hbm_gbs"], 4),
+        "decode": {"per_context": per_point, "gbs": round(dec_gbs, 1),
+                   "rope_us_per_call": round(rope_us, 3), "kv_store_us_per_call": round(store_us, 3)},
+        "roofline": {"kernel": "paged_decode_kernel<128,3>", "bound": "hbm", "achieved": round(dec_gbs, 1),
+                     "peak": peaks["hbm_gbs"], "peak_source": peak_src, "unit": "GB/s",
+                     "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "traffic": traffic_val,
+                     "algorithmic_bytes_per_launch": round(dec_bytes_tot / len(SWEEP)),
+                     "note": "achieved = algorithmic bytes / CUDA-event time of the decode kernel alone "
+                             "(32-layer rotation per context, averaged over the six contexts)"},
+        "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3, 4)},
+        "device_error_word": dev_err,
+    }
+    line["clocks"] = clk.summary()
+    if not args.only_main:
+        line.update(secondary_workloads(dev, peaks, s))
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(sw)
+    del sw
+    return line
+
+
+def secondary_workloads(dev, peaks, s):
+    from paged_kv_cache_188_gb300 import api
+    res = {}
+    # packed ragged prefill (RoPE + KV store + causal paged prefill)
+    pb = W.config4(device=dev)
+    T = pb.q.shape[0]
+    ws = api.alloc_workspace(api.pa_prefill_workspace_bytes(), dev)
+    out = torch.empty_like(pb.q)
+    flops = 4.0 * D * HQ * sum(n * p + n * (n + 1) / 2 for n, p in zip(pb.new_lens, pb.prefix_lens))
+
+    def prefill():
+        api.pa_paged_prefill_attn(pb.q, pb.kv.k_buf, pb.kv.v_buf, 0, pb.qo_indptr, pb.kv_indptr,
+                                  pb.kv.req_to_token, pb.kv.req_pool_indices, pb.scale, ws, out, stream=s)
+    try:
+        prefill()
+        torch.cuda.synchronize()
+        g = capture(prefill, s)
+        ms = time_graph(g, 20, s)
+        tf = flops / (ms * 1e-3) / 1e12
+        res["prefill"] = {"workload": "16 packed prompts, new U[64,2048], prefix U[0,1024], Hq=32 Hkv=8 D=128",
+                          "tokens": T, "causal_tflop": round(flops / 1e12, 4), "ms": round(ms, 4),
+                          "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                          "peak_tflops": peaks["bf16_tflops"]}
+    except api.PaError as e:
+        res["prefill"] = {"unavailable": str(e)}
+    g_rope = capture(lambda: api.pa_rope_packed(pb.q, pb.k_new, pb.positions, pb.cos_tab, pb.sin_tab,
+                                                stream=s), s)
+    ms = time_graph(g_rope, 20, s)
+    res.setdefault("prefill", {})["rope_gbs"] = round(rope_bytes(T) / (ms * 1e-3) / 1e9, 1)
+    g_store = capture(lambda: api.pa_kv_store(pb.kv.k_buf, pb.kv.v_buf, 0, pb.k_new, pb.v_new, pb.loc,
+                                              stream=s), s)
+    ms = time_graph(g_store, 20, s)
+    res["prefill"]["kv_store_gbs"] = round(store_bytes(T) / (ms * 1e-3) / 1e9, 1)
+    del pb
+
+    for name, make, shared in (("decode_b32_shared_prefix", W.config3, True), ("decode_b256_page1", W.config5, False)):
+        st = make(device=dev)
+        B = st.q.shape[0]
+        ws = api.alloc_workspace(api.pa_decode_workspace_bytes(B, st.q.shape[1], HKV, D, MAX_SPLITS), dev)
+        out = torch.empty_like(st.q)
+        q, kn = st.q.clone(), st.k_new.clone()
+
+        def stepf(what=("rope", "store", "decode")):
+            if "rope" in what:
+                api.pa_rope_packed(q, kn, st.positions, st.cos_tab, st.sin_tab, stream=s)
+            if "store" in what:
+                api.pa_kv_store(st.kv.k_buf, st.kv.v_buf, 0, kn, st.v_new, st.loc, stream=s)
+            if "decode" in what:
+                api.pa_paged_decode_attn(q, st.kv.k_buf, st.kv.v_buf, 0, st.kv.req_to_token,
+                                         st.kv.req_pool_indices, st.kv.seq_lens, st.scale, ws, MAX_SPLITS, out,
+                                         stream=s)
+        stepf()
+        torch.cuda.synchronize()
+        g_all = capture(stepf, s)
+        g_dec = capture(lambda: stepf(("decode",)), s)
+        ms_all = time_graph(g_all, 20, s)
+        ms_dec = time_graph(g_dec, 20, s)
+        lens = st.kv.seq_lens.cpu().tolist()
+        Hq = st.q.shape[1]
+        logical = sum(decode_bytes(n, Hq) for n in lens)
+        if shared:
+            unique_tokens = st.kv.used_slots.numel() + B
+            unique = unique_tokens * HKV * D * 4 + sum(n * 4 for n in lens) + B * (Hq * D * 4 + 8)
+        else:
+            unique = logical
+        res[name] = {"batch": B, "sum_seq_len": int(sum(lens)), "step_us": round(ms_all * 1e3, 2),
+                     "decode_us": round(ms_dec * 1e3, 2),
+                     "decode_gbs_unique": round(unique / (ms_dec * 1e-3) / 1e9, 1),
+                     "decode_gbs_logical": round(logical / (ms_dec * 1e-3) / 1e9, 1),
+                     "frac_of_hbm_unique": round(unique / (ms_dec * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        del st, ws, out, q, kn, g_all, g_dec
+        torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def _oracle_layer_call(oracle, k, v, q, kn, vn, n, cos, sin, scale):
+    """One decode layer-call on the oracle: rotary of q/k, store of the new
+    token at its slot (the last row), attention over n tokens."""
+    pos = np.array([n - 1], np.int32)
+    qr, _ = oracle.rope(q, pos, cos, sin)
+    kr, _ = oracle.rope(kn, pos, cos, sin)
+    kb, vb = oracle.kv_store(k, v, 0, kr, vn, np.array([n - 1], np.int32))
+    return oracle.decode(qr, kb, vb, 0, np.arange(n, dtype=np.int32)[None], np.zeros(1, np.int32),
+                         np.array([n], np.int32), scale)
+
+
+def _oracle_inputs(kv, layer, n, q, kn, vn):
+    row = int(kv.req_pool_indices[0])
+    slots = kv.req_to_token[row, :n].long()
+    k = kv.k_buf[layer, slots].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)[None]
+    v = kv.v_buf[layer, slots].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)[None]
+    cv = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    return k, v, cv(q), cv(kn), cv(vn)
+
+
+def cpu_baseline(sw):
+    """The oracle, as it stands, on 4 layers of the six-context sweep (single thread)."""
+    import oracle
+    cos, sin = sw.cos.cpu().numpy(), sw.sin.cpu().numpy()
+    layers = [0, 9, 17, 31]
+    t_tot, b_tot = 0.0, 0
+    for p, n in enumerate(SWEEP):
+        for l in layers:
+            k, v, q, kn, vn = _oracle_inputs(sw.kv, l, n, sw.q[p, l], sw.k_new[p, l], sw.v_new[p, l])
+            t0 = time.perf_counter()
+            _oracle_layer_call(oracle, k, v, q, kn, vn, n, cos, sin, sw.scale)
+            t_tot += time.perf_counter() - t0
+            b_tot += decode_bytes(n) + rope_bytes(1) + store_bytes(1)
+    return {"value": round(b_tot / t_tot / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"layers {layers} of the six-context sweep (24 layer-calls of RoPE + store + decode), "
+                      f"{t_tot:.1f} s single-threaded float64 C; host has {os.cpu_count()} cores"}
+
+
+def run_reference(args, rank, world, local):
+    """The float64 oracle as the reference arm: each step is one layer-call of
+    the sweep (context cycling 1K..32K), timed on one host core."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    if dev.type == "cuda":
+        torch.cuda.set_device(dev)
+    sw = DecodeSweep(dev)
+    cos, sin = sw.cos.cpu().numpy(), sw.sin.cpu().numpy()
+    prepared = []
+    for p, n in enumerate(SWEEP):
+        prepared.append(_oracle_inputs(sw.kv, 17, n, sw.q[p, 17], sw.k_new[p, 17], sw.v_new[p, 17]))
+    for i in range(args.warmup):
+        p = i % len(SWEEP)
+        _oracle_layer_call(oracle, *prepared[p], SWEEP[p], cos, sin, sw.scale)
+    t_tot, b_tot = 0.0, 0
+    for i in range(args.steps):
+        p = i % len(SWEEP)
+        t0 = time.perf_counter()
+        _oracle_layer_call(oracle, *prepared[p], SWEEP[p], cos, sin, sw.scale)
+        t_tot += time.perf_counter() - t0
+        b_tot += decode_bytes(SWEEP[p]) + rope_bytes(1) + store_bytes(1)
+    val = b_tot / t_tot / 1e9
+    return {"metric": "paged decode-attn HBM GB/s (% of peak) & us/layer; packed prefill TFLOP/s",
+            "value": round(val, 4), "unit": "GB/s", "impl": "reference", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t_tot / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "B=1 paged decode layer-call (RoPE + KV store + decode), Hq=32 Hkv=8 D=128, "
+                                   "page 16, contexts cycling 1K-32K (one layer-call per step)"},
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "one layer-call per step, contexts cycling 1K..32K"},
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_profile_case(args):
+    """Small fixed cases for ncu: inputs above the 129 MB L2, a few GB at most."""
+    from paged_kv_cache_188_gb300 import api, build
+    build.build()
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.current_stream(dev)
+    if args.profile == "decode":
+        # 4 requests x 32K tokens, one layer: 512 MiB of K/V per launch
+        st = W.make_decode_step(lens=[32768] * 4, n_q_heads=HQ, n_kv_heads=HKV, head_dim=D, n_layers=1,
+                                size=262144, page_size=PAGE, seed=2, device=dev)
+        api.pa_kv_store(st.kv.k_buf, st.kv.v_buf, 0, st.k_new, st.v_new, st.loc)
+        ws = api.alloc_workspace(api.pa_decode_workspace_bytes(4, HQ, HKV, D, MAX_SPLITS), dev)
+        out = torch.empty_like(st.q)
+        for _ in range(5):
+            api.pa_paged_decode_attn(st.q, st.kv.k_buf, st.kv.v_buf, 0, st.kv.req_to_token, st.kv.req_pool_indices,
+                                     st.kv.seq_lens, st.scale, ws, MAX_SPLITS, out, stream=s)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "decode", "launches": 5, "algorithmic_bytes_per_launch":
+                          4 * decode_bytes(32768), "device_error_word": api.pa_get_error(ws)}))
+    elif args.profile == "prefill":
+        pb = W.config4(device=dev)
+        ws = api.alloc_workspace(api.pa_prefill_workspace_bytes(), dev)
+        out = torch.empty_like(pb.q)
+        api.pa_kv_store(pb.kv.k_buf, pb.kv.v_buf, 0, pb.k_new, pb.v_new, pb.loc)
+        for _ in range(3):
+            api.pa_paged_prefill_attn(pb.q, pb.kv.k_buf, pb.kv.v_buf, 0, pb.qo_indptr, pb.kv_indptr,
+                                      pb.kv.req_to_token, pb.kv.req_pool_indices, pb.scale, ws, out, stream=s)
+        torch.cuda.synchronize()
+        flops = 4.0 * D * HQ * sum(n * p + n * (n + 1) / 2 for n, p in zip(pb.new_lens, pb.prefix_lens))
+        print(json.dumps({"profile": "prefill", "launches": 3, "causal_flops_per_launch": flops,
+                          "device_error_word": api.pa_get_error(ws)}))
+    else:
+        pb = W.config4(device=dev)
+        for _ in range(3):
+            if args.profile == "rope":
+                api.pa_rope_packed(pb.q, pb.k_new, pb.positions, pb.cos_tab, pb.sin_tab, stream=s)
+            else:
+                api.pa_kv_store(pb.kv.k_buf, pb.kv.v_buf, 0, pb.k_new, pb.v_new, pb.loc, stream=s)
+        torch.cuda.synchronize()
+        T = pb.q.shape[0]
+        print(json.dumps({"profile": args.profile, "launches": 3, "algorithmic_bytes_per_launch":
+                          rope_bytes(T) if args.profile == "rope" else store_bytes(T)}))
+
+
+def main():
+    args = parse()
+    if args.profile:
+        run_profile_case(args)
+        return
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world, local)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -429,13 +429,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
                     s_lt[gg] = lt;
                 }
                 __syncthreads();
+                const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
                 for (int e = tid; e < G * D; e += kDecThreads) {
                     const int gg = e / D, d = e - gg * D;
+                    const float *src = a.o_part + ((int64_t)b * a.Hq + hq0 + gg) * D + d;
                     float acc = 0.f;
-                    for (int ss = 0; ss < sb; ++ss) {
-                        const int64_t pr = ((int64_t)ss * a.cap_batch + b) * a.Hq + hq0 + gg;
-                        acc += s_w[ss * G + gg] * __ldcg(a.o_part + pr * D + d);
+                    int ss = 0;
+                    // eight independent loads in flight, summed in split order
+                    for (; ss + 8 <= sb; ss += 8) {
+                        float v[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (ss + j) * split_stride);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc += s_w[(ss + j) * G + gg] * v[j];
                     }
+                    for (; ss < sb; ++ss) acc += s_w[ss * G + gg] * __ldcg(src + ss * split_stride);
                     const float lt = s_lt[gg];
                     a.out[((int64_t)b * a.Hq + hq0 + gg) * D + d] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
                 }

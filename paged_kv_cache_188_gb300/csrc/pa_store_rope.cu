@@ -70,8 +70,12 @@ __global__ void __launch_bounds__(256) rope_kernel(uint4 *__restrict__ q, uint4 
         for (int j = 0; j < 4; ++j) {
             __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162 *>(&w[j]);
             const float x0 = __low2float(pr), x1 = __high2float(pr);
-            const float y0 = fmaf(x0, cc[j], -x1 * ss[j]);
-            const float y1 = fmaf(x0, ss[j], x1 * cc[j]);
+            // x0*c - x1*s and x0*s + x1*c with the second product split exactly
+            // into p + e (FMA remainder), so a cancelling sum keeps its low bits
+            const float p0 = x1 * ss[j], e0 = fmaf(x1, ss[j], -p0);
+            const float p1 = x1 * cc[j], e1 = fmaf(x1, cc[j], -p1);
+            const float y0 = fmaf(x0, cc[j], -p0) - e0;
+            const float y1 = fmaf(x0, ss[j], p1) + e1;
             w[j] = pack_bf16x2(y0, y1);
         }
         *ptr = make_uint4(w[0], w[1], w[2], w[3]);
