@@ -59,6 +59,7 @@ typedef enum {
 #define PA_DEVERR_ROW 0x2       /* a req_pool_indices entry outside [0, req_rows) */
 #define PA_DEVERR_LEN 0x4       /* a seq_len / indptr length outside [0, max_ctx] or n_r > L_r */
 #define PA_DEVERR_POS 0x8       /* a rotary position outside [0, max_pos) */
+#define PA_DEVERR_TIMEOUT 0x10  /* a bounded pipeline wait gave up (internal error); the call aborted */
 
 /* Shape of one of the two KV buffers, bf16 [n_layers, size, n_kv_heads, head_dim];
  * slot `loc` of layer `l` starts at element ((l * size + loc) * n_kv_heads) * head_dim. */
