@@ -7,25 +7,34 @@
 // for request b and query head hq, softmax(scale * q K^T) V over the request's
 // seq_lens[b] cached tokens, K/V rows gathered through req_to_token.
 //
-// How (one kernel, persistent grid of (#SM x resident CTAs)):
+// How (one kernel, one persistent CTA of 8 warps per SM):
 //  * Planning on the device, redundantly in every CTA: sum of seq_lens ->
 //    split length; per request the split count s_b (<= max_splits); a prefix
 //    sum over s_b * Hkv enumerates work items (b, split, kv head).  The grid
 //    never depends on device lengths, so a captured graph stays valid.
-//  * An item loads its token range's slots from req_to_token into shared
-//    memory once, then each of the 4 warps streams 16-token tiles of K and V
-//    (one kv head: 16 rows x 256 B, rows anywhere in the cache) through its own
-//    cp.async ring.  Rows are stored with a 16-byte-chunk XOR swizzle so the
-//    ldmatrix reads below are bank-conflict free.
-//  * QK^T and PV use the warp-level bf16 MMA (m16n8k16): the G query heads of
-//    one kv head form the M=16 rows, so K/V bytes are read once for all G
-//    heads and the fp32 FMA count does not grow with G.  Online softmax in the
-//    log2 domain (exp2), fp32 state per warp.
-//  * The warps' states merge in shared memory; a request with one split writes
-//    bf16 output directly, otherwise the item writes fp32 (o, m, l) partials
-//    and the CTA that completes a (request, kv head) -- an integer atomic
-//    ticket, no waiting -- merges all splits in split order (deterministic),
-//    writes bf16 and re-arms the ticket to zero.
+//  * The CTA's 8 warps share each item: 16-token tile i of the item belongs to
+//    warp i % 8.  Every warp streams its own tiles -- K and V rows of one kv
+//    head, D*2 bytes each wherever the page table puts them -- through a
+//    private ring of S shared-memory stages with 16-byte cp.async copies (D/8
+//    lanes per row, so an instruction reads whole rows).  The ring runs across
+//    item boundaries: while a warp computes its last tiles of one item it is
+//    already loading its first tiles of the next.  Page-table entries of the
+//    next tile to load are prefetched into registers one tile ahead.  Rows are
+//    stored with a 16-byte-chunk XOR swizzle so ldmatrix is conflict free.
+//    (A gather microbenchmark on this GPU: 8 warps x 3 cp.async stages per SM
+//    read these rows at 7.2 TB/s; a single TMA-issuing thread per SM tops out
+//    near 4.4 TB/s.)
+//  * Per tile, warp-level bf16 MMAs (m16n8k16) with tokens as the M dimension:
+//      S^T[tok, head] = K[tok, :] . Q[head, :]       (Q^T held in registers)
+//      online softmax per head column, log2 domain (exp2)
+//      O^T[d, head]  += V^T[d, tok] . P^T[tok, head]   (P^T by movmatrix)
+//    so K/V bytes are read once for all G heads of the kv head.
+//  * At the end of an item the warps' states merge in shared memory; a
+//    request with one split writes bf16 output directly, otherwise the item
+//    writes fp32 (o, m, l) partials and the CTA that completes a (request, kv
+//    head) -- an integer atomic ticket, no waiting -- merges all splits in
+//    split order (deterministic), writes bf16 and re-arms the ticket to zero.
+//  * No spin-waits: cp.async groups and CTA barriers only.
 #include <math.h>
 
 #include "pa_common.cuh"
@@ -33,14 +42,13 @@
 
 namespace pa {
 
-constexpr int kDecWarps = 4;
+constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kDecTile = 16;        // tokens per warp tile
-constexpr int kDecIdxWin = 1024;    // req_to_token entries staged per window
+constexpr int kDecTile = 16;        // tokens per ring stage
 constexpr int kDecMinChunk = 64;    // split length bounds (tokens)
 constexpr int kDecMaxChunk = 1024;
 constexpr int kDecMaxBatch = 4096;
-constexpr int kDecMaxSplits = 256;
+constexpr int kDecMaxSplits = 128;
 
 struct DecodeArgs {
     const __nv_bfloat16 *q;
@@ -83,30 +91,68 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-template <int D, int STAGES>
-struct DecodeSmem {
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kTileBytes = kDecTile * kRowBytes;          // one K or V tile
-    static constexpr int kStageBytes = 2 * kTileBytes;               // K + V
-    static constexpr int kRingBytes = STAGES * kStageBytes;          // per warp
-    static constexpr int kKvBytes = kDecWarps * kRingBytes;
-    static constexpr int kIdxOff = kKvBytes;
-    static constexpr int kPrefOff = kIdxOff + kDecIdxWin * 4;
-    static size_t bytes(int batch) { return (size_t)kPrefOff + (size_t)(batch + 1) * 4; }
+// Shared memory: per-warp rings [warp][S][K tile | V tile], consumer scratch,
+// per-warp stage validity masks, the plan's prefix array.
+template <int D, int S, int NH>
+struct DecSmem {
+    static constexpr int kTile = kDecTile * D * 2;                       // one K or V tile
+    static constexpr int kStage = 2 * kTile;
+    static constexpr int kRing = S * kStage;                             // per warp
+    static constexpr int kScratchOff = kDecWarps * kRing;
+    // warps' states [8][G][D] fp32, later the split merge [sb][G][2] + [sb][G] + [G]
+    static constexpr int kCombine = kDecWarps * 8 * NH * D * 4;
+    static constexpr int kMerge = (3 * kDecMaxSplits * 8 * NH + 8 * NH) * 4;
+    static constexpr int kScratch = kCombine > kMerge ? kCombine : kMerge;
+    static constexpr int kMaskOff = kScratchOff + kScratch;
+    static constexpr int kPrefOff = kMaskOff + kDecWarps * S * 4;
+    static constexpr size_t bytes(int batch) { return (size_t)kPrefOff + (size_t)(batch + 1) * 4; }
+};
+constexpr size_t kSmemLimit = 232448 - 2048;   // opt-in maximum minus static shared memory (with margin)
+
+// Everything an item needs, derived from the plan (identical in every warp).
+struct DecItem {
+    int b, s, h, sb, t0, t1, ntiles;
+    int row;   // -1 if the request row is invalid
 };
 
-template <int D, int STAGES>
+__device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pref, int chunk, int item)
+{
+    int lo = 0, hi = a.batch;   // largest b with s_pref[b] <= item
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pref[mid] <= item) lo = mid; else hi = mid;
+    }
+    DecItem I;
+    I.b = lo;
+    const int local = item - s_pref[lo];
+    I.s = local / a.Hkv;
+    I.h = local - I.s * a.Hkv;
+    int n = clamp_len(__ldg(a.seq_lens + lo), a.max_ctx);
+    int len;
+    split_of(n, chunk, a.max_splits, I.sb, len);
+    I.row = __ldg(a.req_pool_indices + lo);
+    if (I.row < 0 || I.row >= a.req_rows) {
+        I.row = -1;
+        n = 0;
+    }
+    I.t0 = I.s * len;
+    I.t1 = min(n, I.t0 + len);
+    I.ntiles = I.t1 > I.t0 ? (I.t1 - I.t0 + kDecTile - 1) / kDecTile : 0;
+    return I;
+}
+
+template <int D, int S, int NH>
 __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const DecodeArgs a)
 {
-    using L = DecodeSmem<D, STAGES>;
-    constexpr int CPR = D / 8;            // 16-byte chunks per row
-    constexpr int TPI = 32 / CPR;         // rows covered by one warp-wide copy instruction
-    constexpr int COPIES = kDecTile / TPI;
+    using L = DecSmem<D, S, NH>;
     constexpr int KSTEPS = D / 16;
-    constexpr int NT = D / 8;             // n-tiles of the output
+    constexpr int DM = D / 16;         // 16-row d tiles of O^T
+    constexpr int CPR = D / 8;         // 16-byte chunks per row
+    constexpr int TPI = 32 / CPR;      // rows per warp-wide copy instruction
 
     extern __shared__ __align__(128) unsigned char smem[];
-    int32_t *s_idx = reinterpret_cast<int32_t *>(smem + L::kIdxOff);
+    float *scratch = reinterpret_cast<float *>(smem + L::kScratchOff);
+    uint32_t *s_vmask = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
     int32_t *s_pref = reinterpret_cast<int32_t *>(smem + L::kPrefOff);
     __shared__ float s_m[kDecWarps][16], s_l[kDecWarps][16];
     __shared__ int s_red[kDecWarps];
@@ -126,250 +172,251 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
     long long tot = 0;
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) tot += s_red[w];
-    long long want = (tot * Hkv + gridDim.x - 1) / gridDim.x;
+    const long long want = (tot * Hkv + gridDim.x - 1) / gridDim.x;
     int chunk = (int)((want + kDecMinChunk - 1) / kDecMinChunk * kDecMinChunk);
     chunk = chunk < kDecMinChunk ? kDecMinChunk : (chunk > kDecMaxChunk ? kDecMaxChunk : chunk);
-
-    // exclusive prefix of s_b * Hkv over requests; each thread scans a contiguous run
-    const int per = (B + kDecThreads - 1) / kDecThreads;
-    const int b_lo = tid * per, b_hi = min(B, b_lo + per);
-    int run = 0;
-    for (int b = b_lo; b < b_hi; ++b) {
-        int sb, len;
-        split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), chunk, a.max_splits, sb, len);
-        run += sb * Hkv;
-    }
-    int incl = run;
+    {
+        const int per = (B + kDecThreads - 1) / kDecThreads;
+        const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
+        int run = 0;
+        for (int b = b_lo; b < b_hi; ++b) {
+            int sb, len;
+            split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), chunk, a.max_splits, sb, len);
+            run += sb * Hkv;
+        }
+        int incl = run;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        __syncthreads();   // s_red reuse
+        if (lane == 31) s_red[warp] = incl;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += s_red[w];
+        int excl = base + incl - run;
+        for (int b = b_lo; b < b_hi; ++b) {
+            s_pref[b] = excl;
+            int sb, len;
+            split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), chunk, a.max_splits, sb, len);
+            excl += sb * Hkv;
+        }
+        if (tid == kDecThreads - 1) s_pref[B] = base + incl;
     }
-    __syncthreads();   // s_red reuse
-    if (lane == 31) s_red[warp] = incl;
-    __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += s_red[w];
-    int excl = base + incl - run;
-    for (int b = b_lo; b < b_hi; ++b) {
-        s_pref[b] = excl;
-        int sb, len;
-        split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), chunk, a.max_splits, sb, len);
-        excl += sb * Hkv;
-    }
-    if (tid == kDecThreads - 1) s_pref[B] = base + incl;
     __syncthreads();
     const int total_items = s_pref[B];
+    const int64_t slot_stride = (int64_t)Hkv * D;
+    const uint32_t ring = smem_u32(smem) + warp * L::kRing;
 
-    const uint32_t ring = smem_u32(smem) + warp * L::kRingBytes;
+    // ------------------------------------------- this warp's load cursor
+    // walks (item, tile) pairs in the order the warp computes them: tiles
+    // warp, warp+8, ... of the CTA's items blockIdx.x, blockIdx.x+gridDim.x, ...
+    int ld_item = blockIdx.x, ld_tile = warp;
+    DecItem LI;
+    LI.ntiles = 0;
+    LI.row = -1;
+    LI.t0 = LI.t1 = LI.h = 0;
+    if (ld_item < total_items) LI = dec_item(a, s_pref, chunk, ld_item);
+    auto ld_settle = [&]() {   // move the cursor to the next tile that exists
+        while (ld_item < total_items && ld_tile >= LI.ntiles) {
+            ld_item += gridDim.x;
+            ld_tile = warp;
+            if (ld_item < total_items) LI = dec_item(a, s_pref, chunk, ld_item);
+        }
+    };
+    ld_settle();
+    // page-table entry of token `lane` (lanes < 16) of the cursor's tile
+    int pf_slot = -1;
+    auto ld_prefetch = [&]() {
+        pf_slot = -1;
+        if (ld_item < total_items && lane < kDecTile && LI.row >= 0) {
+            const int tok = LI.t0 + ld_tile * kDecTile + lane;
+            if (tok < LI.t1) pf_slot = __ldg(a.req_to_token + (int64_t)LI.row * a.max_ctx + tok);
+        }
+    };
+    ld_prefetch();
+    int n_issued = 0;
+    // issue the cursor's tile into ring stage n_issued % S, then advance
+    auto issue = [&]() {
+        if (ld_item >= total_items) return;
+        const int st = n_issued % S;
+        const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile;
+        const int tok0 = LI.t0 + ld_tile * kDecTile;
+        int sl = pf_slot;
+        const bool in_range = lane < kDecTile && tok0 + lane < LI.t1;
+        if (in_range && (sl < 0 || sl >= a.size)) set_error(a.err, PA_DEVERR_SLOT);
+        const bool ok = in_range && sl >= 0 && sl < a.size;
+        if (!ok) sl = -1;
+        const unsigned vmask = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) s_vmask[warp * S + st] = vmask;
+        const __nv_bfloat16 *kh = a.k_layer + (int64_t)LI.h * D;
+        const __nv_bfloat16 *vh = a.v_layer + (int64_t)LI.h * D;
+#pragma unroll
+        for (int j = 0; j < kDecTile / TPI; ++j) {
+            const int r = j * TPI + lane / CPR;
+            const int ch = lane % CPR;
+            const int rs = __shfl_sync(0xffffffffu, sl, r);
+            const int64_t off = rs >= 0 ? (int64_t)rs * slot_stride + ch * 8 : 0;
+            const int nb = rs >= 0 ? 16 : 0;      // masked rows: zero fill, no read
+            const uint32_t o = r * (D * 2) + ((ch ^ (r & 7)) << 4);
+            cp_async_16(kb + o, kh + off, nb);
+            cp_async_16(vb + o, vh + off, nb);
+        }
+        ++n_issued;
+        ld_tile += kDecWarps;
+        ld_settle();
+        ld_prefetch();
+    };
 
+#pragma unroll
+    for (int i = 0; i < S - 1; ++i) {
+        issue();
+        cp_async_commit();
+    }
+
+    int n_done = 0;   // tiles computed by this warp
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        // ------------------------------------------------ item -> (b, s, h)
-        int lo = 0, hi = B;   // largest b with s_pref[b] <= item
-        while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
-            if (s_pref[mid] <= item) lo = mid; else hi = mid;
-        }
-        const int b = lo;
-        const int local = item - s_pref[b];
-        const int s = local / Hkv, h = local - s * Hkv;
-        int n = __ldg(a.seq_lens + b);
-        if (n < 0 || n > a.max_ctx) {
-            if (tid == 0 && s == 0 && h == 0) set_error(a.err, PA_DEVERR_LEN);
-            n = clamp_len(n, a.max_ctx);
-        }
-        int sb, len;
-        split_of(n, chunk, a.max_splits, sb, len);
-        const int row = __ldg(a.req_pool_indices + b);
-        if (row < 0 || row >= a.req_rows) {
-            if (tid == 0 && s == 0 && h == 0) set_error(a.err, PA_DEVERR_ROW);
-            n = 0;    // treated as empty: zeros out
-        }
-        const int t0 = s * len, t1 = min(n, t0 + len);
-        const int32_t *r2t = a.req_to_token + (int64_t)(row < 0 || row >= a.req_rows ? 0 : row) * a.max_ctx;
-
-        // query fragments: rows = the G heads of kv head h, zero beyond G
-        uint32_t qa[KSTEPS][4];
+        const DecItem I = dec_item(a, s_pref, chunk, item);
+        const int hq0 = I.h * G;
+        // Q^T as the MMA's B operand: n = head (8 per n-tile), k = d
+        uint32_t qb[KSTEPS][NH][2];
         {
-            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(a.q + ((int64_t)b * a.Hq + h * G) * D);
+            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(a.q + ((int64_t)I.b * a.Hq + hq0) * D);
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int c0 = kk * 8 + t4;     // 32-bit column index (pairs of bf16)
-                qa[kk][0] = g < G ? __ldg(q32 + g * (D / 2) + c0) : 0u;
-                qa[kk][1] = g + 8 < G ? __ldg(q32 + (g + 8) * (D / 2) + c0) : 0u;
-                qa[kk][2] = g < G ? __ldg(q32 + g * (D / 2) + c0 + 4) : 0u;
-                qa[kk][3] = g + 8 < G ? __ldg(q32 + (g + 8) * (D / 2) + c0 + 4) : 0u;
+            for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt) {
+                    const int hd = nt * 8 + g;
+                    qb[kk][nt][0] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + t4) : 0u;
+                    qb[kk][nt][1] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + 4 + t4) : 0u;
+                }
+        }
+        float o[DM][NH][4];
+#pragma unroll
+        for (int i = 0; i < DM; ++i)
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) o[i][nt][0] = o[i][nt][1] = o[i][nt][2] = o[i][nt][3] = 0.f;
+        float m[NH][2], l[NH][2];
+#pragma unroll
+        for (int nt = 0; nt < NH; ++nt) m[nt][0] = m[nt][1] = -INFINITY, l[nt][0] = l[nt][1] = 0.f;
+
+        for (int i = warp; i < I.ntiles; i += kDecWarps) {
+            issue();
+            cp_async_commit();
+            cp_async_wait<S - 1>();
+            __syncwarp();
+            const int st = n_done % S;
+            const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile;
+            const uint32_t vmask = s_vmask[warp * S + st];
+            // S^T = K Q^T (16 tokens x 8 heads per n-tile)
+            float sc[NH][4];
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            {
+                const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int c_hi = lane >> 4;
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    uint32_t af[4];
+                    ldmatrix_x4(kb + r * (D * 2) + (((kk * 2 + c_hi) ^ (r & 7)) << 4), af[0], af[1], af[2], af[3]);
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt) mma_bf16_16816(sc[nt], af, qb[kk][nt][0], qb[kk][nt][1]);
+                }
             }
+            // mask, scale; column (head) maxima over the 16 tokens
+            const bool ok0 = (vmask >> g) & 1u, ok1 = (vmask >> (g + 8)) & 1u;
+            float mr[NH][2], al[NH][2];
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) {
+                sc[nt][0] = ok0 ? sc[nt][0] * a.scale_log2 : -INFINITY;
+                sc[nt][1] = ok0 ? sc[nt][1] * a.scale_log2 : -INFINITY;
+                sc[nt][2] = ok1 ? sc[nt][2] * a.scale_log2 : -INFINITY;
+                sc[nt][3] = ok1 ? sc[nt][3] * a.scale_log2 : -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float v = fmaxf(sc[nt][j], sc[nt][j + 2]);
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                    const float mn = fmaxf(m[nt][j], v);
+                    mr[nt][j] = mn == -INFINITY ? 0.f : mn;
+                    al[nt][j] = ex2(m[nt][j] - mr[nt][j]);
+                    m[nt][j] = mn;
+                }
+            }
+            // P = exp2(s - m), lane-partial column sums, P^T fragments
+            uint32_t pb[NH][2];
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) {
+                const float p0 = ex2(sc[nt][0] - mr[nt][0]);
+                const float p1 = ex2(sc[nt][1] - mr[nt][1]);
+                const float p2 = ex2(sc[nt][2] - mr[nt][0]);
+                const float p3 = ex2(sc[nt][3] - mr[nt][1]);
+                l[nt][0] = l[nt][0] * al[nt][0] + (p0 + p2);
+                l[nt][1] = l[nt][1] * al[nt][1] + (p1 + p3);
+                pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+                pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+            }
+#pragma unroll
+            for (int dm = 0; dm < DM; ++dm)
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt) {
+                    o[dm][nt][0] *= al[nt][0];
+                    o[dm][nt][1] *= al[nt][1];
+                    o[dm][nt][2] *= al[nt][0];
+                    o[dm][nt][3] *= al[nt][1];
+                }
+            // O^T += V^T P^T: V^T fragments by transposing ldmatrix of the V rows
+            {
+                const int r = ((lane >> 4) & 1) * 8 + (lane & 7);
+                const int c_lo = (lane >> 3) & 1;
+#pragma unroll
+                for (int dm = 0; dm < DM; ++dm) {
+                    uint32_t af[4];
+                    ldmatrix_x4_trans(vb + r * (D * 2) + (((dm * 2 + c_lo) ^ (r & 7)) << 4), af[0], af[1], af[2],
+                                      af[3]);
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt) mma_bf16_16816(o[dm][nt], af, pb[nt][0], pb[nt][1]);
+                }
+            }
+            __syncwarp();
+            ++n_done;
         }
 
-        float o_acc[NT][4];
+        // ------------------------------------- merge the warps' states
 #pragma unroll
-        for (int i = 0; i < NT; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-        const __nv_bfloat16 *kh = a.k_layer + (int64_t)h * D;
-        const __nv_bfloat16 *vh = a.v_layer + (int64_t)h * D;
-        const int64_t slot_stride = (int64_t)Hkv * D;
-
-        for (int w0 = t0; w0 < t1; w0 += kDecIdxWin) {
-            const int nwin = min(kDecIdxWin, t1 - w0);
-            __syncthreads();
-            for (int i = tid; i < nwin; i += kDecThreads) {
-                int sl = __ldg(r2t + w0 + i);
-                if (sl < 0 || sl >= a.size) {
-                    set_error(a.err, PA_DEVERR_SLOT);
-                    sl = -1;
-                }
-                s_idx[i] = sl;
+        for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 4);
+                l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 8);
+                l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 16);
             }
-            __syncthreads();
-
-            const int n_tiles = (nwin + kDecTile - 1) / kDecTile;
-            const int my_tiles = n_tiles > warp ? (n_tiles - warp + kDecWarps - 1) / kDecWarps : 0;
-
-            auto issue = [&](int it) {
-                const int tile = warp + it * kDecWarps;
-                const uint32_t st_base = ring + (it % STAGES) * L::kStageBytes;
+        __syncthreads();   // scratch free: the previous item is done with it
+        if (g == 0) {
 #pragma unroll
-                for (int c = 0; c < COPIES; ++c) {
-                    const int r = c * TPI + lane / CPR;     // row within tile
-                    const int ch = lane % CPR;
-                    const int tok = tile * kDecTile + r;
-                    const int sl = tok < nwin ? s_idx[tok] : -1;
-                    const int64_t off = sl >= 0 ? (int64_t)sl * slot_stride + ch * 8 : 0;
-                    const int nb = sl >= 0 ? 16 : 0;
-                    const uint32_t dst = st_base + r * L::kRowBytes + ((ch ^ (r & 7)) << 4);
-                    cp_async_16(dst, kh + off, nb);
-                    cp_async_16(dst + L::kTileBytes, vh + off, nb);
-                }
-            };
-
+            for (int nt = 0; nt < NH; ++nt)
 #pragma unroll
-            for (int i = 0; i < STAGES - 1; ++i) {
-                if (i < my_tiles) issue(i);
-                cp_async_commit();
-            }
-            for (int it = 0; it < my_tiles; ++it) {
-                if (it + STAGES - 1 < my_tiles) issue(it + STAGES - 1);
-                cp_async_commit();
-                cp_async_wait<STAGES - 1>();
-                __syncwarp();
-
-                const int tile = warp + it * kDecWarps;
-                const uint32_t kb = ring + (it % STAGES) * L::kStageBytes;
-                const uint32_t vb = kb + L::kTileBytes;
-
-                // S = Q K^T for 16 tokens (two n-tiles of 8)
-                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                {
-                    const int mi = lane >> 3;
-                    const int r = ((mi >> 1) << 3) + (lane & 7);
-#pragma unroll
-                    for (int kk = 0; kk < KSTEPS; ++kk) {
-                        const int ch = kk * 2 + (mi & 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(kb + r * L::kRowBytes + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
-                        mma_bf16_16816(sc[0], qa[kk], b0, b1);
-                        mma_bf16_16816(sc[1], qa[kk], b2, b3);
+                for (int j = 0; j < 2; ++j) {
+                    const int hd = nt * 8 + 2 * t4 + j;
+                    if (hd < G) {
+                        s_m[warp][hd] = m[nt][j];
+                        s_l[warp][hd] = l[nt][j];
                     }
                 }
-                // mask + online softmax (log2 domain)
-                float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tok = tile * kDecTile + nt * 8 + 2 * t4 + e;
-                        const bool ok = tok < nwin && s_idx[tok] >= 0;
-                        sc[nt][e] = ok ? sc[nt][e] * a.scale_log2 : -INFINITY;
-                        sc[nt][e + 2] = ok ? sc[nt][e + 2] * a.scale_log2 : -INFINITY;
-                        mx0 = fmaxf(mx0, sc[nt][e]);
-                        mx1 = fmaxf(mx1, sc[nt][e + 2]);
-                    }
-                }
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float mr0 = mn0 == -INFINITY ? 0.f : mn0;
-                const float mr1 = mn1 == -INFINITY ? 0.f : mn1;
-                const float al0 = ex2(m0 - mr0), al1 = ex2(m1 - mr1);
-                m0 = mn0;
-                m1 = mn1;
-                float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    sc[nt][0] = ex2(sc[nt][0] - mr0);
-                    sc[nt][1] = ex2(sc[nt][1] - mr0);
-                    sc[nt][2] = ex2(sc[nt][2] - mr1);
-                    sc[nt][3] = ex2(sc[nt][3] - mr1);
-                    ps0 += sc[nt][0] + sc[nt][1];
-                    ps1 += sc[nt][2] + sc[nt][3];
-                }
-                l0 = l0 * al0 + ps0;
-                l1 = l1 * al1 + ps1;
-#pragma unroll
-                for (int i = 0; i < NT; ++i) {
-                    o_acc[i][0] *= al0;
-                    o_acc[i][1] *= al0;
-                    o_acc[i][2] *= al1;
-                    o_acc[i][3] *= al1;
-                }
-                uint32_t pa_[4];
-                pa_[0] = pack_bf16x2(sc[0][0], sc[0][1]);
-                pa_[1] = pack_bf16x2(sc[0][2], sc[0][3]);
-                pa_[2] = pack_bf16x2(sc[1][0], sc[1][1]);
-                pa_[3] = pack_bf16x2(sc[1][2], sc[1][3]);
-                // O += P V
-                {
-                    const int mi = lane >> 3;
-                    const int r = ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                    for (int np = 0; np < D / 16; ++np) {
-                        const int ch = np * 2 + (mi >> 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(vb + r * L::kRowBytes + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
-                        mma_bf16_16816(o_acc[2 * np], pa_, b0, b1);
-                        mma_bf16_16816(o_acc[2 * np + 1], pa_, b2, b3);
-                    }
-                }
-                __syncwarp();
-            }
-            cp_async_wait<0>();
-        }
-
-        // ---------------------------------------- merge the warps' states
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-        __syncthreads();   // every warp is done with its ring: reuse it as scratch
-        float *s_o = reinterpret_cast<float *>(smem);   // [warps][G][D]
-        if (t4 == 0) {
-            if (g < G) {
-                s_m[warp][g] = m0;
-                s_l[warp][g] = l0;
-            }
-            if (g + 8 < G) {
-                s_m[warp][g + 8] = m1;
-                s_l[warp][g + 8] = l1;
-            }
         }
 #pragma unroll
-        for (int i = 0; i < NT; ++i) {
-            const int d = i * 8 + 2 * t4;
-            if (g < G) {
-                s_o[(warp * G + g) * D + d] = o_acc[i][0];
-                s_o[(warp * G + g) * D + d + 1] = o_acc[i][1];
-            }
-            if (g + 8 < G) {
-                s_o[(warp * G + g + 8) * D + d] = o_acc[i][2];
-                s_o[(warp * G + g + 8) * D + d + 1] = o_acc[i][3];
-            }
-        }
+        for (int dm = 0; dm < DM; ++dm)
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int hd = nt * 8 + 2 * t4 + (e & 1);
+                    const int d = dm * 16 + g + 8 * (e >> 1);
+                    if (hd < G) scratch[(warp * G + hd) * D + d] = o[dm][nt][e];
+                }
         __syncthreads();
-        const int hq0 = h * G;
         for (int e = tid; e < G * D; e += kDecThreads) {
             const int gg = e / D, d = e - gg * D;
             float M = -INFINITY;
@@ -381,12 +428,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
             for (int w = 0; w < kDecWarps; ++w) {
                 const float wt = ex2(s_m[w][gg] - Mr);
                 lsum += wt * s_l[w][gg];
-                acc += wt * s_o[(w * G + gg) * D + d];
+                acc += wt * scratch[(w * G + gg) * D + d];
             }
-            if (sb == 1) {
-                a.out[((int64_t)b * a.Hq + hq0 + gg) * D + d] = __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
+            if (I.sb == 1) {
+                a.out[((int64_t)I.b * a.Hq + hq0 + gg) * D + d] = __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
             } else {
-                const int64_t pr = ((int64_t)s * a.cap_batch + b) * a.Hq + hq0 + gg;
+                const int64_t pr = ((int64_t)I.s * a.cap_batch + I.b) * a.Hq + hq0 + gg;
                 a.o_part[pr * D + d] = acc;
                 if (d == 0) {
                     a.ml_part[pr * 2] = M;
@@ -394,24 +441,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
                 }
             }
         }
-
-        if (sb > 1) {
+        if (I.sb > 1) {
             // ------------------------- last CTA of (b, h) merges the splits
-            __threadfence();
+            // the barrier orders every thread's partial stores before thread
+            // 0's gpu-scope fence, which (being cumulative) publishes them all
+            // before the ticket
             __syncthreads();
             if (tid == 0) {
-                const int prev = atomicAdd(a.counters + b * Hkv + h, 1);
-                s_flag = prev == sb - 1;
+                __threadfence();
+                const int prev = atomicAdd(a.counters + I.b * Hkv + I.h, 1);
+                s_flag = prev == I.sb - 1;
                 __threadfence();
             }
             __syncthreads();
             if (s_flag) {
-                float *s_ml = reinterpret_cast<float *>(smem);            // [sb][G][2]
-                float *s_w = s_ml + 2 * kDecMaxSplits * 16;                // [sb][G]
-                float *s_lt = s_w + kDecMaxSplits * 16;                    // [G]
+                const int sb = I.sb;
+                float *s_ml = scratch;             // [sb][G][2]
+                float *s_w = s_ml + 2 * sb * G;    // [sb][G]
+                float *s_lt = s_w + sb * G;        // [G]
                 for (int i = tid; i < sb * G; i += kDecThreads) {
                     const int ss = i / G, gg = i - ss * G;
-                    const int64_t pr = ((int64_t)ss * a.cap_batch + b) * a.Hq + hq0 + gg;
+                    const int64_t pr = ((int64_t)ss * a.cap_batch + I.b) * a.Hq + hq0 + gg;
                     s_ml[i * 2] = __ldcg(a.ml_part + pr * 2);
                     s_ml[i * 2 + 1] = __ldcg(a.ml_part + pr * 2 + 1);
                 }
@@ -432,11 +482,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
                 const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
                 for (int e = tid; e < G * D; e += kDecThreads) {
                     const int gg = e / D, d = e - gg * D;
-                    const float *src = a.o_part + ((int64_t)b * a.Hq + hq0 + gg) * D + d;
+                    const float *src = a.o_part + ((int64_t)I.b * a.Hq + hq0 + gg) * D + d;
                     float acc = 0.f;
                     int ss = 0;
-                    // eight independent loads in flight, summed in split order
-                    for (; ss + 8 <= sb; ss += 8) {
+                    for (; ss + 8 <= sb; ss += 8) {   // eight loads in flight, summed in split order
                         float v[8];
 #pragma unroll
                         for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (ss + j) * split_stride);
@@ -445,33 +494,40 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
                     }
                     for (; ss < sb; ++ss) acc += s_w[ss * G + gg] * __ldcg(src + ss * split_stride);
                     const float lt = s_lt[gg];
-                    a.out[((int64_t)b * a.Hq + hq0 + gg) * D + d] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
+                    a.out[((int64_t)I.b * a.Hq + hq0 + gg) * D + d] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
                 }
-                if (tid == 0) a.counters[b * Hkv + h] = 0;
+                if (tid == 0) a.counters[I.b * Hkv + I.h] = 0;
             }
         }
-        __syncthreads();
     }
+    cp_async_wait<0>();
 }
 
-template <int D, int STAGES>
+template <int D, int S, int NH>
 static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
 {
-    auto kern = paged_decode_kernel<D, STAGES>;
-    const size_t smem = DecodeSmem<D, STAGES>::bytes(a.batch);
+    auto kern = paged_decode_kernel<D, S, NH>;
+    const size_t smem = DecSmem<D, S, NH>::bytes(a.batch);
+    if (smem > kSmemLimit) return PA_ERR_UNSUPPORTED;
     static size_t configured = 0;
     if (smem > configured) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return PA_ERR_CUDA;
         configured = smem;
     }
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecThreads, smem) != cudaSuccess || occ < 1)
-        return PA_ERR_CUDA;
-    const int grid = num_sms() * occ;
-    kern<<<grid, kDecThreads, smem, st>>>(a);
+    kern<<<num_sms(), kDecThreads, smem, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
+
+// Deepest ring whose shared memory fits this batch.
+template <int D, int NH>
+static pa_status dispatch_decode(const DecodeArgs &a, cudaStream_t st)
+{
+    if (DecSmem<D, 4, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 4, NH>(a, st);
+    if (DecSmem<D, 3, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 3, NH>(a, st);
+    return launch_decode<D, 2, NH>(a, st);
+}
+static_assert(DecSmem<128, 2, 2>::bytes(kDecMaxBatch) <= kSmemLimit, "decode smem at the largest batch");
 
 }  // namespace pa
 
@@ -525,6 +581,6 @@ extern "C" pa_status pa_paged_decode_attn(const void *q, int batch, int n_q_head
     a.cap_batch = ws.cap_batch;
     a.max_splits = max_splits;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    if (s.head_dim == 128) return launch_decode<128, 3>(a, st);
-    return launch_decode<64, 4>(a, st);
+    if (s.head_dim == 128) return G > 8 ? dispatch_decode<128, 2>(a, st) : dispatch_decode<128, 1>(a, st);
+    return G > 8 ? dispatch_decode<64, 2>(a, st) : dispatch_decode<64, 1>(a, st);
 }

@@ -1,6 +1,7 @@
 // pa_internal.h -- host-side helpers shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -19,6 +20,13 @@ inline bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) &
 
 // SM count of the current device (cached per device; a property, not call state).
 int num_sms();
+
+// Encode a TMA tensor map over a bf16 tensor of `rank` (<= 3) dimensions
+// (dims innermost first, strides in bytes for dims 1..rank-1) with the given
+// box, 128-byte swizzle, zero fill out of range.  The driver entry point is
+// resolved once through the runtime (no libcuda link).  false on failure.
+bool encode_tmap_bf16(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                      const cuuint32_t *box);
 
 // Decode workspace geometry, a pure function of its arguments.
 struct DecodeWsLayout {

@@ -7,22 +7,24 @@
 // request r (position p_r + i, p_r = cached prefix) attends to positions
 // 0 .. p_r + i of the request, K/V rows read through req_to_token.
 //
-// How (persistent, one CTA per SM, warp-specialised, 192 threads):
+// How (persistent, one CTA per SM, warp-specialised, 320 threads):
 //  * Work item = (request, q-tile, kv head).  A q-tile packs the G query heads
 //    of one kv head into the MMA's M = 128 rows: 128/G consecutive tokens x G
 //    heads (token-major), so each K/V tile fetched serves all G heads.
-//  * warp 4 (producer): TMA.  Q tile via a 3-D tensor map (d, head, token);
+//  * warp 8 (producer): TMA.  Q tile via a 3-D tensor map (d, head, token);
 //    K/V tiles of 128 positions gathered through req_to_token: a group of 16
 //    positions on 16 consecutive slots (one page) is one 16-row box per 64-wide
 //    half, anything else falls back to 1-row boxes; positions past the item's
 //    last visible key load zeros (out-of-range rows).  128-byte swizzle, the
 //    layout the UMMA descriptors below expect.  Two K and two V stages.
-//  * warp 5 (MMA issuer, one thread): S = Q K^T into one of two TMEM buffers
+//  * warp 9 (MMA issuer, one thread): S = Q K^T into one of two TMEM buffers
 //    (128 lanes x 128 fp32 columns), O += P V into a third; commits signal the
 //    other warps.  S(t+1) is issued before PV(t) so the tensor core works on
 //    the next scores while the softmax warps finish the current tile.
-//  * warps 0-3 (softmax + epilogue, thread i owns row i = TMEM lane i): read S
-//    with tcgen05.ld, causal mask (bottom-right aligned), online softmax in the
+//  * warps 0-7 (softmax + epilogue): row i = TMEM lane i, warpgroup h owns
+//    columns [64h, 64h+64) of S, O and P; the two halves of a row exchange
+//    their maxima (and at the end their sums) through shared memory.  Causal
+//    mask (bottom-right aligned) only on diagonal tiles, online softmax in the
 //    log2 domain with a lazy running max (O in TMEM is rescaled only when the
 //    max grows by more than 2^8), P rounded to bf16 into shared memory as the
 //    A operand of the PV MMA.  Epilogue: O / l to bf16, rows of padding tokens
@@ -41,7 +43,9 @@ using namespace sm100;
 constexpr int kPfRows = 128;           // MMA M: rows of a q tile
 constexpr int kPfKeys = 128;           // keys per kv tile
 constexpr int kPfD = 128;              // head dim
-constexpr int kPfThreads = 192;
+constexpr int kPfSoftmaxThreads = 256;  // warps 0-7: two warpgroups, one per 64-column half
+constexpr int kPfThreads = 320;         // + warp 8 (TMA producer) + warp 9 (MMA issuer)
+constexpr int kWarpProducer = 8, kWarpMma = 9;
 constexpr int kPfMaxReqs = 2048;
 constexpr int kHalf = 128 * 128;       // one 128-row x 128-byte swizzled half tile (16 KB)
 constexpr int kOffQ = 0;               // 2 halves
@@ -50,9 +54,10 @@ constexpr int kOffV = 6 * kHalf;       // 2 stages x 2 halves
 constexpr int kOffP = 10 * kHalf;      // 2 halves
 constexpr int kOffBar = 12 * kHalf;
 enum { Q_FULL, Q_EMPTY, K_FULL, K_FULL1, K_EMPTY, K_EMPTY1, V_FULL, V_FULL1, V_EMPTY, V_EMPTY1,
-       S_FULL, S_FULL1, S_EMPTY, S_EMPTY1, P_FULL, O_DONE, O_EMPTY, N_BARS };
+       S_FULL, S_FULL1, S_EMPTY, S_EMPTY1, P_FULL, O_DONE, O_EMPTY, XCH0, XCH1, XCH2, XCH3, N_BARS };
 constexpr int kOffMisc = kOffBar + 32 * 8;
-constexpr int kOffPref = kOffMisc + 64;
+constexpr int kOffXch = kOffMisc + 64;            // row max / sum exchange between the two halves
+constexpr int kOffPref = kOffXch + 3 * 128 * 4 * 2;
 constexpr uint32_t kTmemCols = 512;    // S0 | S1 | O | unused
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);   // Q (K-major) x K (K-major)
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (K-major) x V (MN-major)
@@ -120,7 +125,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP;
     volatile int *s_abort = reinterpret_cast<volatile int *>(sb + kOffMisc);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sb + kOffMisc + 4);
-    int *s_wsum = reinterpret_cast<int *>(sb + kOffMisc + 8);    // 6 ints
+    int *s_wsum = reinterpret_cast<int *>(sb + kOffMisc + 8);    // one int per warp
     int *s_pref = reinterpret_cast<int *>(sb + kOffPref);
     auto bar = [&](int i) -> uint32_t { return base + kOffBar + i * 8; };
 
@@ -130,13 +135,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     if (tid == 0) {
         *s_abort = 0;
         for (int i = 0; i < N_BARS; ++i) {
-            const uint32_t cnt = (i == S_EMPTY || i == S_EMPTY1 || i == P_FULL || i == O_EMPTY) ? 128u : 1u;
+            const uint32_t cnt = (i == S_EMPTY || i == S_EMPTY1 || i == P_FULL || i == O_EMPTY)
+                                     ? (uint32_t)kPfSoftmaxThreads
+                                     : (i >= XCH0 ? 64u : 1u);
             mbar_init(bar(i), cnt);
         }
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(smem_u32(s_tmem), kTmemCols);
-    if (warp == 4 && lane == 0) {
+    if (warp == kWarpMma) tmem_alloc(smem_u32(s_tmem), kTmemCols);
+    if (warp == kWarpProducer && lane == 0) {
         prefetch_tmap(&p.tm_q);
         prefetch_tmap(&p.tm_k16);
         prefetch_tmap(&p.tm_k1);
@@ -194,7 +201,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     const int total_items = s_pref[p.R];
     const int G = p.G;
 
-    if (warp == 4) {
+    if (warp == kWarpProducer) {
         // ================================================== TMA producer
         int kt = 0, it = 0;
         bool ok = true;
@@ -267,7 +274,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 issue(&p.tm_v16, &p.tm_v1, sV + st * 2 * kHalf, bar(V_FULL + st));
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ================================================== MMA issuer
         if (lane == 0) {
             int kt = 0, it = 0;
@@ -325,15 +332,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         }
         __syncwarp();
     } else {
-        // ======================================== softmax + epilogue (rows)
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const uint32_t o_addr = tmem + lane_base + 256;
+        // ============================ softmax + epilogue (row, column half)
+        // thread -> row (TMEM lane) and one 64-column half of S, O and P
+        const int half = warp >> 2;
+        const int row = tid & 127;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t o_addr = tmem + lane_base + 256 + half * 64;
+        float *xmax = reinterpret_cast<float *>(sb + kOffXch);     // [parity][half][row]
+        float *xsum = xmax + 4 * 128;                              // [half][row]
+        const uint32_t xbar = bar(XCH0 + (warp & 3));
+        uint32_t xph = 0;
         const float sl2 = p.scale_log2;
         int kt = 0;
         bool ok = true;
         for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
             const PfItem I = pf_item(p, s_pref, item);
-            const int tok = tid / G;                    // token of this row within the q tile
+            const int tok = row / G;                    // token of this row within the q tile
             const int qpos = I.p + I.q0 + tok;           // its position in the request
             float m_run = -INFINITY, l_run = 0.f;
             for (int t = 0; t < I.ntiles; ++t, ++kt) {
@@ -343,18 +357,46 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                     break;
                 }
                 tc_fence_after();
-                const uint32_t s_addr = tmem + lane_base + st * 128;
-                const int limit = qpos - t * kPfKeys;    // columns <= limit are visible
-                uint32_t r[32];
-                float mx = -INFINITY;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    tmem_ld32(s_addr + ch * 32, r);
+                uint32_t r[64];
+                {
+                    uint32_t (&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+                    uint32_t (&r1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+                    const uint32_t s_addr = tmem + lane_base + st * 128 + half * 64;
+                    tmem_ld32(s_addr, r0);
+                    tmem_ld32(s_addr + 32, r1);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (ch * 32 + c <= limit) mx = fmaxf(mx, __uint_as_float(r[c]));
                 }
+                const int limit = qpos - t * kPfKeys - half * 64;    // columns <= limit are visible
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                if (limit >= 63) {
+#pragma unroll
+                    for (int c = 0; c < 64; c += 4) {
+                        mx0 = fmaxf(mx0, __uint_as_float(r[c]));
+                        mx1 = fmaxf(mx1, __uint_as_float(r[c + 1]));
+                        mx2 = fmaxf(mx2, __uint_as_float(r[c + 2]));
+                        mx3 = fmaxf(mx3, __uint_as_float(r[c + 3]));
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const float v = c <= limit ? __uint_as_float(r[c]) : -INFINITY;
+                        r[c] = __float_as_uint(v);
+                        if ((c & 3) == 0) mx0 = fmaxf(mx0, v);
+                        if ((c & 3) == 1) mx1 = fmaxf(mx1, v);
+                        if ((c & 3) == 2) mx2 = fmaxf(mx2, v);
+                        if ((c & 3) == 3) mx3 = fmaxf(mx3, v);
+                    }
+                }
+                float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                // row maximum across the two halves
+                xmax[((kt & 1) * 2 + half) * 128 + row] = mx;
+                mbar_arrive(xbar);
+                if (!mbar_wait(xbar, xph & 1, s_abort, err, PA_DEVERR_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                ++xph;
+                mx = fmaxf(mx, xmax[((kt & 1) * 2 + (half ^ 1)) * 128 + row]);
                 float m_new = m_run;
                 bool rescale = false;
                 if (mx > m_run && (m_run == -INFINITY || (mx - m_run) * sl2 > 8.f)) {
@@ -364,22 +406,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 const float alpha = rescale ? ex2f((m_run - m_new) * sl2) : 1.f;
                 m_run = m_new;
                 const float mb = m_new == -INFINITY ? 0.f : m_new * sl2;
-                uint32_t pk[64];
-                float sum = 0.f;
+                uint32_t pk[32];
+                float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    tmem_ld32(s_addr + ch * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const float v0 = (ch * 32 + c <= limit) ? ex2f(fmaf(__uint_as_float(r[c]), sl2, -mb)) : 0.f;
-                        const float v1 =
-                            (ch * 32 + c + 1 <= limit) ? ex2f(fmaf(__uint_as_float(r[c + 1]), sl2, -mb)) : 0.f;
-                        sum += v0 + v1;
-                        pk[ch * 16 + c / 2] = pack_bf16x2(v0, v1);
-                    }
+                for (int c = 0; c < 64; c += 2) {
+                    const float v0 = ex2f(fmaf(__uint_as_float(r[c]), sl2, -mb));
+                    const float v1 = ex2f(fmaf(__uint_as_float(r[c + 1]), sl2, -mb));
+                    sum0 += v0;
+                    sum1 += v1;
+                    pk[c / 2] = pack_bf16x2(v0, v1);
                 }
-                l_run = l_run * alpha + sum;
+                l_run = l_run * alpha + (sum0 + sum1);
                 tc_fence_before();
                 mbar_arrive(bar(S_EMPTY + st));
                 // the previous PV must be done: P's buffer is free and O is stable
@@ -390,25 +427,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 tc_fence_after();
                 if (t > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        tmem_ld32(o_addr + ch * 32, r);
+                    for (int ch = 0; ch < 2; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld32(o_addr + ch * 32, o);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-                        tmem_st32(o_addr + ch * 32, r);
+                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st32(o_addr + ch * 32, o);
                     }
                     tmem_wait_st();
                 }
-                // P row -> shared memory, K-major 128-byte swizzle (chunk ^ row % 8)
-                unsigned char *prow = sb + kOffP + tid * 128;
+                // P: this half's 64 keys of the row -> its K-major 128-byte swizzled region
+                unsigned char *prow = sb + kOffP + half * kHalf + row * 128;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 v = make_uint4(pk[hh * 32 + c * 4], pk[hh * 32 + c * 4 + 1], pk[hh * 32 + c * 4 + 2],
-                                                   pk[hh * 32 + c * 4 + 3]);
-                        *reinterpret_cast<uint4 *>(prow + hh * kHalf + ((c ^ (tid & 7)) << 4)) = v;
-                    }
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(prow + ((c ^ (row & 7)) << 4)) =
+                        make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bar(P_FULL));
@@ -417,23 +451,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
             // ------------------------------------------------ epilogue
             if (!mbar_wait(bar(O_DONE), (kt - 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
             tc_fence_after();
-            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+            xsum[half * 128 + row] = l_run;
+            mbar_arrive(xbar);
+            if (!mbar_wait(xbar, xph & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
+            ++xph;
+            const float l_tot = l_run + xsum[(half ^ 1) * 128 + row];
+            const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const bool row_ok = tok < I.nq;
             __nv_bfloat16 *dst =
-                p.out + ((int64_t)(I.qs + I.q0 + tok) * p.Hq + I.h * G + (tid - tok * G)) * kPfD;
-            uint32_t r[32];
+                p.out + ((int64_t)(I.qs + I.q0 + tok) * p.Hq + I.h * G + (row - tok * G)) * kPfD + half * 64;
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                tmem_ld32(o_addr + ch * 32, r);
+            for (int ch = 0; ch < 2; ++ch) {
+                uint32_t o[32];
+                tmem_ld32(o_addr + ch * 32, o);
                 tmem_wait_ld();
                 if (row_ok) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(r[q * 8 + 0]) * inv_l, __uint_as_float(r[q * 8 + 1]) * inv_l);
-                        v.y = pack_bf16x2(__uint_as_float(r[q * 8 + 2]) * inv_l, __uint_as_float(r[q * 8 + 3]) * inv_l);
-                        v.z = pack_bf16x2(__uint_as_float(r[q * 8 + 4]) * inv_l, __uint_as_float(r[q * 8 + 5]) * inv_l);
-                        v.w = pack_bf16x2(__uint_as_float(r[q * 8 + 6]) * inv_l, __uint_as_float(r[q * 8 + 7]) * inv_l);
+                        v.x = pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv_l, __uint_as_float(o[q * 8 + 1]) * inv_l);
+                        v.y = pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv_l, __uint_as_float(o[q * 8 + 3]) * inv_l);
+                        v.z = pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv_l, __uint_as_float(o[q * 8 + 5]) * inv_l);
+                        v.w = pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv_l, __uint_as_float(o[q * 8 + 7]) * inv_l);
                         *reinterpret_cast<uint4 *>(dst + ch * 32 + q * 8) = v;
                     }
                 }
@@ -444,40 +483,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     }
 
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
 }
 
 // ------------------------------------------------------------------ host
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
 static bool encode(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
                    const cuuint32_t *box)
 {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tmap_bf16(m, ptr, rank, dims, strides, box);
 }
 
 }  // namespace pa

@@ -72,7 +72,7 @@ def test_decode_host_validation(lib):
     assert _decode(lib, s=_shape(d=96)) == 4                 # unsupported head_dim
     assert _decode(lib, hq=64) == 4                          # G = 32 > 16
     assert _decode(lib, splits=0) == 2
-    assert _decode(lib, splits=257) == 2
+    assert _decode(lib, splits=129) == 2
     assert _decode(lib, batch=4097) == 2
     assert _decode(lib, ws=0) == 1
     assert _decode(lib, ws=FAKE + 16) == 3                   # workspace must be 256-byte aligned
