@@ -164,6 +164,38 @@ pa_status pa_paged_decode_attn(const void *q, int batch, int n_q_heads, const vo
                                float scale, void *workspace, size_t workspace_bytes,
                                int max_splits, void *out, cudaStream_t st);
 
+/* ------------------------------------------- decode attn, no allocation
+ * No counterpart on the pages: an addition for callers that cannot hand the
+ * library a workspace.  Some callers have no way to allocate device memory
+ * at the point where decode runs -- a plugin inside a host program that owns
+ * every device allocation, or a serving loop that forbids cudaMalloc because
+ * it synchronises the device and stalls every stream -- and this entry point
+ * serves them.  It computes exactly what pa_paged_decode_attn computes (same
+ * arguments, same results bit for bit for the same max_splits), but its
+ * scratch (split partials, merge tickets, error word) is a fixed 16 MiB array
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  It allocates nothing itself and calls no allocating routine.
+ *   - Size limit: the partials of `batch` requests must fit the 16 MiB:
+ *     16 MiB >= 1024 + batch * (n_kv_heads*4 + max_splits*n_q_heads*(head_dim+2)*4)
+ *     (e.g. 15 requests at Hq=32, head_dim 128, max_splits 64); larger calls
+ *     return PA_ERR_WORKSPACE and enqueue nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call clears the error word and the merge tickets on `st` before
+ *     its kernel, so a call never sees the previous call's state; the array
+ *     otherwise keeps the last call's contents.  All calls on all streams of a
+ *     device share the one array: calls that may overlap on the GPU race and
+ *     must be serialised by the caller (e.g. one stream).
+ *   - error_word (device pointer, may be NULL) receives a copy of the call's
+ *     device error word (PA_DEVERR_* bits) on `st`. */
+pa_status pa_paged_decode_attn_noalloc(const void *q, int batch, int n_q_heads, const void *k_buf,
+                                       const void *v_buf, pa_kv_shape s, int layer_id,
+                                       const int32_t *req_to_token, int req_rows, int max_ctx,
+                                       const int32_t *req_pool_indices, const int32_t *seq_lens,
+                                       float scale, int max_splits, void *out, int32_t *error_word,
+                                       cudaStream_t st);
+
 /* ----------------------------------------------------------- prefill attn
  * Commit e58a728: packed prompts with a shared prefix start in one forward,
  * paged prefill (attn_paged_prefill), rows located by cumulative query lengths;

@@ -39,7 +39,7 @@ class KvShape(ctypes.Structure):
 
 EXPORTS = ["pa_status_string", "pa_decode_workspace_bytes", "pa_prefill_workspace_bytes",
            "pa_workspace_init", "pa_get_error", "pa_get_error_word", "pa_kv_store", "pa_rope_packed",
-           "pa_paged_decode_attn", "pa_paged_prefill_attn"]
+           "pa_paged_decode_attn", "pa_paged_prefill_attn", "pa_paged_decode_attn_noalloc"]
 
 _lib = None
 
@@ -69,6 +69,8 @@ def lib():
                                        P, P]
     L.pa_paged_prefill_attn.argtypes = [P, i32, i32, P, P, KvShape, i32, P, P, i32, P, i32, i32, P, f32, P,
                                         sz, P, P]
+    L.pa_paged_decode_attn_noalloc.argtypes = [P, i32, i32, P, P, KvShape, i32, P, i32, i32, P, P, f32, i32, P,
+                                               P, P]
     for name in EXPORTS[3:]:
         getattr(L, name).restype = i32
     _lib = L
@@ -194,6 +196,26 @@ def pa_paged_decode_attn(q, k_buf, v_buf, layer_id, req_to_token, req_pool_indic
         _p(q), B, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(req_to_token), req_to_token.shape[0],
         req_to_token.shape[1], _p(req_pool_indices), _p(seq_lens), float(scale), _p(workspace),
         workspace.numel(), max_splits, _p(out), _stream(stream)))
+
+
+def pa_paged_decode_attn_noalloc(q, k_buf, v_buf, layer_id, req_to_token, req_pool_indices, seq_lens, scale,
+                                 max_splits, out, error_word=None, stream=None):
+    """pa_paged_decode_attn with the library's fixed internal scratch instead of a workspace."""
+    s = _kv_shape(k_buf, v_buf)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(req_to_token, torch.int32, "req_to_token", 2)
+    _need(req_pool_indices, torch.int32, "req_pool_indices", 1)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    if error_word is not None:
+        _need(error_word, torch.int32, "error_word")
+    B, Hq, D = q.shape
+    if out.shape != q.shape or D != s.head_dim or req_pool_indices.numel() != B or seq_lens.numel() != B:
+        raise ValueError("q/out [batch, n_q_heads, head_dim], req_pool_indices/seq_lens [batch] expected")
+    _ok("pa_paged_decode_attn_noalloc", lib().pa_paged_decode_attn_noalloc(
+        _p(q), B, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(req_to_token), req_to_token.shape[0],
+        req_to_token.shape[1], _p(req_pool_indices), _p(seq_lens), float(scale), max_splits, _p(out),
+        _p(error_word), _stream(stream)))
 
 
 def pa_paged_prefill_attn(q, k_buf, v_buf, layer_id, qo_indptr, kv_indptr, req_to_token, req_pool_indices,
