@@ -37,10 +37,11 @@
 //  * No spin-waits: cp.async groups and CTA barriers only.
 #include <math.h>
 
-#include "pa_common.cuh"
 #include "pa_internal.h"
+#include "pa_sm100.cuh"
 
 namespace pa {
+using namespace sm100;
 
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
@@ -51,6 +52,8 @@ constexpr int kDecMaxBatch = 4096;
 constexpr int kDecMaxSplits = 128;
 
 struct DecodeArgs {
+    CUtensorMap tm_k;    // 2-D (element, row) over k_buf rows, 64 x 16 boxes, 128-byte swizzle
+    CUtensorMap tm_v;
     const __nv_bfloat16 *q;
     const __nv_bfloat16 *k_layer;
     const __nv_bfloat16 *v_layer;
@@ -65,6 +68,7 @@ struct DecodeArgs {
     int batch, Hq, Hkv, G;
     int size, req_rows, max_ctx;
     int cap_batch, max_splits;
+    int layer_row0;      // layer_id * size: tensor-map row of slot 0 of the layer
     float scale_log2;
 };
 
@@ -91,21 +95,32 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// Shared memory: per-warp rings [warp][S][K tile | V tile], consumer scratch,
-// per-warp stage validity masks, the plan's prefix array.
+// Shared memory (from a 1024-byte aligned base): per-warp rings
+// [warp][S][K tile | V tile], each tile D/64 halves of 16 rows x 128 B with the
+// 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)) -- the
+// layout TMA writes and the cp.async path reproduces; consumer scratch;
+// per-warp stage validity masks and mbarriers; the plan's prefix array.
 template <int D, int S, int NH>
 struct DecSmem {
-    static constexpr int kTile = kDecTile * D * 2;                       // one K or V tile
+    static constexpr int kHalf = kDecTile * 128;                         // 16 rows x 128 B
+    static constexpr int kTile = (D / 64) * kHalf;                       // one K or V tile
     static constexpr int kStage = 2 * kTile;
     static constexpr int kRing = S * kStage;                             // per warp
     static constexpr int kScratchOff = kDecWarps * kRing;
-    // warps' states [8][G][D] fp32, later the split merge [sb][G][2] + [sb][G] + [G]
-    static constexpr int kCombine = kDecWarps * 8 * NH * D * 4;
+    // half the warps' O states [4][G][D] fp32 at a time, later the split merge
+    // [sb][G][2] + [sb][G] + [G]
+    static constexpr int kCombine = (kDecWarps / 2) * 8 * NH * D * 4;
     static constexpr int kMerge = (3 * kDecMaxSplits * 8 * NH + 8 * NH) * 4;
     static constexpr int kScratch = kCombine > kMerge ? kCombine : kMerge;
     static constexpr int kMaskOff = kScratchOff + kScratch;
-    static constexpr int kPrefOff = kMaskOff + kDecWarps * S * 4;
-    static constexpr size_t bytes(int batch) { return (size_t)kPrefOff + (size_t)(batch + 1) * 4; }
+    static constexpr int kBarOff = kMaskOff + kDecWarps * S * 4;
+    static constexpr int kPrefOff = kBarOff + kDecWarps * S * 8;
+    static constexpr size_t bytes(int batch) { return 1024 + (size_t)kPrefOff + (size_t)(batch + 1) * 4; }
+    // byte offset of 16-byte chunk c of row r inside a K or V tile
+    __device__ static __forceinline__ uint32_t off(int r, int c)
+    {
+        return (uint32_t)((c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    }
 };
 constexpr size_t kSmemLimit = 232448 - 2048;   // opt-in maximum minus static shared memory (with margin)
 
@@ -142,7 +157,7 @@ __device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pr
 }
 
 template <int D, int S, int NH>
-__global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __grid_constant__ DecodeArgs a)
 {
     using L = DecSmem<D, S, NH>;
     constexpr int KSTEPS = D / 16;
@@ -150,17 +165,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
     constexpr int CPR = D / 8;         // 16-byte chunks per row
     constexpr int TPI = 32 / CPR;      // rows per warp-wide copy instruction
 
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + (((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw));
     float *scratch = reinterpret_cast<float *>(smem + L::kScratchOff);
     uint32_t *s_vmask = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
     int32_t *s_pref = reinterpret_cast<int32_t *>(smem + L::kPrefOff);
     __shared__ float s_m[kDecWarps][16], s_l[kDecWarps][16];
     __shared__ int s_red[kDecWarps];
-    __shared__ int s_flag;
+    __shared__ int s_flag, s_pend[3];
+    __shared__ int s_abort_storage;
+    volatile int *s_abort = &s_abort_storage;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
     const int B = a.batch, Hkv = a.Hkv, G = a.G;
+    const uint32_t bars = smem_u32(smem + L::kBarOff) + warp * S * 8;   // this warp's stage barriers
+    if (lane == 0) {
+        // 32 lanes' cp.async completions + lane 0's arrival carrying the TMA bytes
+        for (int i = 0; i < S; ++i) mbar_init(bars + i * 8, 33);
+        fence_mbar_init();
+    }
+    if (tid == 0) *s_abort = 0;
 
     // ---------------------------------------------------------- planning
     int my_tot = 0;
@@ -208,72 +233,154 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
     const int total_items = s_pref[B];
     const int64_t slot_stride = (int64_t)Hkv * D;
     const uint32_t ring = smem_u32(smem) + warp * L::kRing;
+    bool bad = false;   // a ring wait timed out: skip work, keep the barriers
 
-    // ------------------------------------------- this warp's load cursor
-    // walks (item, tile) pairs in the order the warp computes them: tiles
-    // warp, warp+8, ... of the CTA's items blockIdx.x, blockIdx.x+gridDim.x, ...
-    int ld_item = blockIdx.x, ld_tile = warp;
-    DecItem LI;
-    LI.ntiles = 0;
-    LI.row = -1;
-    LI.t0 = LI.t1 = LI.h = 0;
-    if (ld_item < total_items) LI = dec_item(a, s_pref, chunk, ld_item);
-    auto ld_settle = [&]() {   // move the cursor to the next tile that exists
-        while (ld_item < total_items && ld_tile >= LI.ntiles) {
-            ld_item += gridDim.x;
-            ld_tile = warp;
-            if (ld_item < total_items) LI = dec_item(a, s_pref, chunk, ld_item);
+    // ------------------------------------------- this warp's load cursors
+    // a cursor walks (item, tile) pairs in the order the warp computes them:
+    // tiles warp, warp+8, ... of the CTA's items blockIdx.x, +gridDim.x, ...
+    // `cur` is the next tile to load, `nxt` the one after; both hold their
+    // page-table entries (lane t < 16: token t), fetched when the cursor moved
+    struct Cursor {
+        int item, tile, slot;
+        DecItem I;
+    };
+    auto settle = [&](Cursor &c) {
+        while (c.item < total_items && c.tile >= c.I.ntiles) {
+            c.item += gridDim.x;
+            c.tile = warp;
+            if (c.item < total_items) c.I = dec_item(a, s_pref, chunk, c.item);
+        }
+        c.slot = -1;
+        if (c.item < total_items && lane < kDecTile && c.I.row >= 0) {
+            const int tok = c.I.t0 + c.tile * kDecTile + lane;
+            if (tok < c.I.t1) c.slot = __ldg(a.req_to_token + (int64_t)c.I.row * a.max_ctx + tok);
         }
     };
-    ld_settle();
-    // page-table entry of token `lane` (lanes < 16) of the cursor's tile
-    int pf_slot = -1;
-    auto ld_prefetch = [&]() {
-        pf_slot = -1;
-        if (ld_item < total_items && lane < kDecTile && LI.row >= 0) {
-            const int tok = LI.t0 + ld_tile * kDecTile + lane;
-            if (tok < LI.t1) pf_slot = __ldg(a.req_to_token + (int64_t)LI.row * a.max_ctx + tok);
-        }
-    };
-    ld_prefetch();
+    Cursor cur;
+    cur.item = blockIdx.x;
+    cur.tile = warp;
+    cur.I.ntiles = 0;
+    cur.I.row = -1;
+    cur.I.t0 = cur.I.t1 = cur.I.h = 0;
+    if (cur.item < total_items) cur.I = dec_item(a, s_pref, chunk, cur.item);
+    settle(cur);
+    Cursor nxt = cur;
+    nxt.tile += kDecWarps;
+    settle(nxt);
     int n_issued = 0;
-    // issue the cursor's tile into ring stage n_issued % S, then advance
+    // load the `cur` tile into ring stage n_issued % S, then advance both cursors
     auto issue = [&]() {
-        if (ld_item >= total_items) return;
+        if (cur.item >= total_items) return;
         const int st = n_issued % S;
-        const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile;
-        const int tok0 = LI.t0 + ld_tile * kDecTile;
-        int sl = pf_slot;
-        const bool in_range = lane < kDecTile && tok0 + lane < LI.t1;
+        const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile, fb = bars + st * 8;
+        const int tok0 = cur.I.t0 + cur.tile * kDecTile;
+        int sl = cur.slot;
+        const bool in_range = lane < kDecTile && tok0 + lane < cur.I.t1;
         if (in_range && (sl < 0 || sl >= a.size)) set_error(a.err, PA_DEVERR_SLOT);
         const bool ok = in_range && sl >= 0 && sl < a.size;
         if (!ok) sl = -1;
         const unsigned vmask = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0) s_vmask[warp * S + st] = vmask;
-        const __nv_bfloat16 *kh = a.k_layer + (int64_t)LI.h * D;
-        const __nv_bfloat16 *vh = a.v_layer + (int64_t)LI.h * D;
-#pragma unroll
-        for (int j = 0; j < kDecTile / TPI; ++j) {
-            const int r = j * TPI + lane / CPR;
-            const int ch = lane % CPR;
-            const int rs = __shfl_sync(0xffffffffu, sl, r);
-            const int64_t off = rs >= 0 ? (int64_t)rs * slot_stride + ch * 8 : 0;
-            const int nb = rs >= 0 ? 16 : 0;      // masked rows: zero fill, no read
-            const uint32_t o = r * (D * 2) + ((ch ^ (r & 7)) << 4);
-            cp_async_16(kb + o, kh + off, nb);
-            cp_async_16(vb + o, vh + off, nb);
+        // 16 tokens on 16 consecutive slots (one page): four TMA boxes
+        const int s0 = __shfl_sync(0xffffffffu, sl, 0);
+        const bool page = (__ballot_sync(0xffffffffu, ok && sl == s0 + lane) & 0xFFFFu) == 0xFFFFu;
+        if (lane == 0) {
+            s_vmask[warp * S + st] = vmask;
+            mbar_arrive_expect_tx(fb, page ? 2u * L::kTile : 0u);
         }
+        __syncwarp();
+        const int h = cur.I.h;
+        if (page) {
+            if (lane == 0) {
+#pragma unroll
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    tma_load_2d(kb + hh * L::kHalf, &a.tm_k, h * D + hh * 64, a.layer_row0 + s0, fb);
+                    tma_load_2d(vb + hh * L::kHalf, &a.tm_v, h * D + hh * 64, a.layer_row0 + s0, fb);
+                }
+            }
+        } else {
+            const __nv_bfloat16 *kh = a.k_layer + (int64_t)h * D;
+            const __nv_bfloat16 *vh = a.v_layer + (int64_t)h * D;
+#pragma unroll
+            for (int j = 0; j < kDecTile / TPI; ++j) {
+                const int r = j * TPI + lane / CPR;
+                const int ch = lane % CPR;
+                const int rs = __shfl_sync(0xffffffffu, sl, r);
+                const int64_t off = rs >= 0 ? (int64_t)rs * slot_stride + ch * 8 : 0;
+                const int nb = rs >= 0 ? 16 : 0;      // masked rows: zero fill, no read
+                const uint32_t o = L::off(r, ch);
+                cp_async_16(kb + o, kh + off, nb);
+                cp_async_16(vb + o, vh + off, nb);
+            }
+        }
+        cp_async_arrive_noinc(fb);
         ++n_issued;
-        ld_tile += kDecWarps;
-        ld_settle();
-        ld_prefetch();
+        cur = nxt;
+        nxt.tile += kDecWarps;
+        settle(nxt);
     };
 
 #pragma unroll
-    for (int i = 0; i < S - 1; ++i) {
-        issue();
-        cp_async_commit();
-    }
+    for (int i = 0; i < S - 1; ++i) issue();
+
+    // ------------------------------------------------------ split merge
+    // The CTA whose ticket completes (b, h) merges all its splits in split
+    // order, writes bf16 and re-arms the ticket.  Whole-CTA; uses the scratch.
+    int pend_prev = -1;                        // thread 0: pending ticket result
+    auto merge_splits = [&](int b, int h, int sb) {
+        const int hq0 = h * G;
+        float *s_ml = scratch;             // [sb][G][2]
+        float *s_w = s_ml + 2 * sb * G;    // [sb][G]
+        float *s_lt = s_w + sb * G;        // [G]
+        for (int i = tid; i < sb * G; i += kDecThreads) {
+            const int ss = i / G, gg = i - ss * G;
+            const int64_t pr = ((int64_t)ss * a.cap_batch + b) * a.Hq + hq0 + gg;
+            s_ml[i * 2] = __ldcg(a.ml_part + pr * 2);
+            s_ml[i * 2 + 1] = __ldcg(a.ml_part + pr * 2 + 1);
+        }
+        __syncthreads();
+        for (int gg = tid; gg < G; gg += kDecThreads) {
+            float M = -INFINITY;
+            for (int ss = 0; ss < sb; ++ss) M = fmaxf(M, s_ml[(ss * G + gg) * 2]);
+            const float Mr = M == -INFINITY ? 0.f : M;
+            float lt = 0.f;
+            for (int ss = 0; ss < sb; ++ss) {
+                const float wt = ex2(s_ml[(ss * G + gg) * 2] - Mr);
+                s_w[ss * G + gg] = wt;
+                lt += wt * s_ml[(ss * G + gg) * 2 + 1];
+            }
+            s_lt[gg] = lt;
+        }
+        __syncthreads();
+        const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
+        for (int e = tid; e < G * D; e += kDecThreads) {
+            const int gg = e / D, d = e - gg * D;
+            const float *src = a.o_part + ((int64_t)b * a.Hq + hq0 + gg) * D + d;
+            float acc = 0.f;
+            int ss = 0;
+            for (; ss + 8 <= sb; ss += 8) {   // eight loads in flight, summed in split order
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (ss + j) * split_stride);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc += s_w[(ss + j) * G + gg] * v[j];
+            }
+            for (; ss < sb; ++ss) acc += s_w[ss * G + gg] * __ldcg(src + ss * split_stride);
+            const float lt = s_lt[gg];
+            a.out[((int64_t)b * a.Hq + hq0 + gg) * D + d] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
+        }
+        if (tid == 0) a.counters[b * Hkv + h] = 0;
+        __syncthreads();
+    };
+    // examine the pending ticket (whole CTA): merge if this CTA was last
+    auto resolve_ticket = [&]() {
+        if (tid == 0) {
+            s_flag = pend_prev >= 0 && pend_prev == s_pend[2] - 1;
+            if (s_flag) fence_acq_rel_gpu();   // acquire: the other CTAs' partials are visible
+            pend_prev = -1;
+        }
+        __syncthreads();
+        if (s_flag) merge_splits(s_pend[0], s_pend[1], s_pend[2]);
+    };
 
     int n_done = 0;   // tiles computed by this warp
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
@@ -302,27 +409,37 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
         for (int nt = 0; nt < NH; ++nt) m[nt][0] = m[nt][1] = -INFINITY, l[nt][0] = l[nt][1] = 0.f;
 
         for (int i = warp; i < I.ntiles; i += kDecWarps) {
-            issue();
-            cp_async_commit();
-            cp_async_wait<S - 1>();
-            __syncwarp();
+            if (!bad) issue();
             const int st = n_done % S;
+            if (!bad && !mbar_wait(bars + st * 8, (n_done / S) & 1, s_abort, a.err, PA_DEVERR_TIMEOUT)) bad = true;
+            ++n_done;
+            if (bad) continue;
             const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile;
             const uint32_t vmask = s_vmask[warp * S + st];
             // S^T = K Q^T (16 tokens x 8 heads per n-tile)
-            float sc[NH][4];
+            float sc[NH][4], sc2[NH][4];   // two independent accumulation chains (even / odd k)
 #pragma unroll
-            for (int nt = 0; nt < NH; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            for (int nt = 0; nt < NH; ++nt) {
+                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                sc2[nt][0] = sc2[nt][1] = sc2[nt][2] = sc2[nt][3] = 0.f;
+            }
             {
                 const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
                 const int c_hi = lane >> 4;
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk) {
                     uint32_t af[4];
-                    ldmatrix_x4(kb + r * (D * 2) + (((kk * 2 + c_hi) ^ (r & 7)) << 4), af[0], af[1], af[2], af[3]);
+                    ldmatrix_x4(kb + L::off(r, kk * 2 + c_hi), af[0], af[1], af[2], af[3]);
 #pragma unroll
-                    for (int nt = 0; nt < NH; ++nt) mma_bf16_16816(sc[nt], af, qb[kk][nt][0], qb[kk][nt][1]);
+                    for (int nt = 0; nt < NH; ++nt) {
+                        if (kk & 1) mma_bf16_16816(sc2[nt], af, qb[kk][nt][0], qb[kk][nt][1]);
+                        else mma_bf16_16816(sc[nt], af, qb[kk][nt][0], qb[kk][nt][1]);
+                    }
                 }
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[nt][e] += sc2[nt][e];
             }
             // mask, scale; column (head) maxima over the 16 tokens
             const bool ok0 = (vmask >> g) & 1u, ok1 = (vmask >> (g + 8)) & 1u;
@@ -374,14 +491,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
 #pragma unroll
                 for (int dm = 0; dm < DM; ++dm) {
                     uint32_t af[4];
-                    ldmatrix_x4_trans(vb + r * (D * 2) + (((dm * 2 + c_lo) ^ (r & 7)) << 4), af[0], af[1], af[2],
-                                      af[3]);
+                    ldmatrix_x4_trans(vb + L::off(r, dm * 2 + c_lo), af[0], af[1], af[2], af[3]);
 #pragma unroll
                     for (int nt = 0; nt < NH; ++nt) mma_bf16_16816(o[dm][nt], af, pb[nt][0], pb[nt][1]);
                 }
             }
             __syncwarp();
-            ++n_done;
         }
 
         // ------------------------------------- merge the warps' states
@@ -393,7 +508,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
                 l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 8);
                 l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 16);
             }
-        __syncthreads();   // scratch free: the previous item is done with it
+        // scratch free (the previous item is done with it); all warps stop
+        // together if any ring wait timed out
+        if (__syncthreads_or(bad)) break;
+        resolve_ticket();   // the previous item's split merge, if this CTA completed it
         if (g == 0) {
 #pragma unroll
             for (int nt = 0; nt < NH; ++nt)
@@ -406,101 +524,91 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const Deco
                     }
                 }
         }
+        // O states go through the scratch in two rounds (warps 0-3, then 4-7);
+        // every element still sums warps 0..7 in order with the same weights
+        constexpr int EPT = (8 * NH * D + kDecThreads - 1) / kDecThreads;
+        float acc[EPT], lsum[EPT], Mx[EPT];
 #pragma unroll
-        for (int dm = 0; dm < DM; ++dm)
+        for (int rr = 0; rr < 2; ++rr) {
+            if (rr == 1) __syncthreads();   // round 0 readers are done with the scratch
+            if ((warp >> 2) == rr) {
+                const int wl = warp & 3;
 #pragma unroll
-            for (int nt = 0; nt < NH; ++nt)
+                for (int dm = 0; dm < DM; ++dm)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int hd = nt * 8 + 2 * t4 + (e & 1);
-                    const int d = dm * 16 + g + 8 * (e >> 1);
-                    if (hd < G) scratch[(warp * G + hd) * D + d] = o[dm][nt][e];
-                }
-        __syncthreads();
-        for (int e = tid; e < G * D; e += kDecThreads) {
-            const int gg = e / D, d = e - gg * D;
-            float M = -INFINITY;
+                    for (int nt = 0; nt < NH; ++nt)
 #pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, s_m[w][gg]);
-            const float Mr = M == -INFINITY ? 0.f : M;
-            float lsum = 0.f, acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) {
-                const float wt = ex2(s_m[w][gg] - Mr);
-                lsum += wt * s_l[w][gg];
-                acc += wt * scratch[(w * G + gg) * D + d];
+                        for (int e = 0; e < 4; ++e) {
+                            const int hd = nt * 8 + 2 * t4 + (e & 1);
+                            const int d = dm * 16 + g + 8 * (e >> 1);
+                            if (hd < G) scratch[(wl * G + hd) * D + d] = o[dm][nt][e];
+                        }
             }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < EPT; ++k) {
+                const int e = tid + k * kDecThreads;
+                if (e >= G * D) continue;
+                const int gg = e / D, d = e - gg * D;
+                if (rr == 0) {
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, s_m[w][gg]);
+                    Mx[k] = M;
+                    acc[k] = 0.f;
+                    lsum[k] = 0.f;
+                }
+                const float Mr = Mx[k] == -INFINITY ? 0.f : Mx[k];
+#pragma unroll
+                for (int w = 0; w < kDecWarps / 2; ++w) {
+                    const int wg = rr * (kDecWarps / 2) + w;
+                    const float wt = ex2(s_m[wg][gg] - Mr);
+                    lsum[k] += wt * s_l[wg][gg];
+                    acc[k] += wt * scratch[(w * G + gg) * D + d];
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int e = tid + k * kDecThreads;
+            if (e >= G * D) continue;
+            const int gg = e / D, d = e - gg * D;
             if (I.sb == 1) {
-                a.out[((int64_t)I.b * a.Hq + hq0 + gg) * D + d] = __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
+                a.out[((int64_t)I.b * a.Hq + hq0 + gg) * D + d] =
+                    __float2bfloat16_rn(lsum[k] > 0.f ? acc[k] / lsum[k] : 0.f);
             } else {
                 const int64_t pr = ((int64_t)I.s * a.cap_batch + I.b) * a.Hq + hq0 + gg;
-                a.o_part[pr * D + d] = acc;
+                a.o_part[pr * D + d] = acc[k];
                 if (d == 0) {
-                    a.ml_part[pr * 2] = M;
-                    a.ml_part[pr * 2 + 1] = lsum;
+                    a.ml_part[pr * 2] = Mx[k];
+                    a.ml_part[pr * 2 + 1] = lsum[k];
                 }
             }
         }
         if (I.sb > 1) {
-            // ------------------------- last CTA of (b, h) merges the splits
-            // the barrier orders every thread's partial stores before thread
-            // 0's gpu-scope fence, which (being cumulative) publishes them all
-            // before the ticket
+            // ticket for (b, h): the barrier orders every thread's partial
+            // stores before thread 0's release-ordered atomic; its result is
+            // only examined at the next item end (or at exit), so the round
+            // trip overlaps the next item's tiles
             __syncthreads();
             if (tid == 0) {
-                __threadfence();
-                const int prev = atomicAdd(a.counters + I.b * Hkv + I.h, 1);
-                s_flag = prev == I.sb - 1;
-                __threadfence();
-            }
-            __syncthreads();
-            if (s_flag) {
-                const int sb = I.sb;
-                float *s_ml = scratch;             // [sb][G][2]
-                float *s_w = s_ml + 2 * sb * G;    // [sb][G]
-                float *s_lt = s_w + sb * G;        // [G]
-                for (int i = tid; i < sb * G; i += kDecThreads) {
-                    const int ss = i / G, gg = i - ss * G;
-                    const int64_t pr = ((int64_t)ss * a.cap_batch + I.b) * a.Hq + hq0 + gg;
-                    s_ml[i * 2] = __ldcg(a.ml_part + pr * 2);
-                    s_ml[i * 2 + 1] = __ldcg(a.ml_part + pr * 2 + 1);
-                }
-                __syncthreads();
-                for (int gg = tid; gg < G; gg += kDecThreads) {
-                    float M = -INFINITY;
-                    for (int ss = 0; ss < sb; ++ss) M = fmaxf(M, s_ml[(ss * G + gg) * 2]);
-                    const float Mr = M == -INFINITY ? 0.f : M;
-                    float lt = 0.f;
-                    for (int ss = 0; ss < sb; ++ss) {
-                        const float wt = ex2(s_ml[(ss * G + gg) * 2] - Mr);
-                        s_w[ss * G + gg] = wt;
-                        lt += wt * s_ml[(ss * G + gg) * 2 + 1];
-                    }
-                    s_lt[gg] = lt;
-                }
-                __syncthreads();
-                const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
-                for (int e = tid; e < G * D; e += kDecThreads) {
-                    const int gg = e / D, d = e - gg * D;
-                    const float *src = a.o_part + ((int64_t)I.b * a.Hq + hq0 + gg) * D + d;
-                    float acc = 0.f;
-                    int ss = 0;
-                    for (; ss + 8 <= sb; ss += 8) {   // eight loads in flight, summed in split order
-                        float v[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (ss + j) * split_stride);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) acc += s_w[(ss + j) * G + gg] * v[j];
-                    }
-                    for (; ss < sb; ++ss) acc += s_w[ss * G + gg] * __ldcg(src + ss * split_stride);
-                    const float lt = s_lt[gg];
-                    a.out[((int64_t)I.b * a.Hq + hq0 + gg) * D + d] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
-                }
-                if (tid == 0) a.counters[I.b * Hkv + I.h] = 0;
+                pend_prev = atom_add_release_gpu(a.counters + I.b * Hkv + I.h, 1);
+                s_pend[0] = I.b;
+                s_pend[1] = I.h;
+                s_pend[2] = I.sb;
             }
         }
     }
-    cp_async_wait<0>();
+    if (!bad && !*s_abort) resolve_ticket();
+    if (bad || *s_abort) {
+        // aborted: let this warp's loads already in flight land before the
+        // CTA's shared memory goes away (bounded, 10 ms per stage)
+        for (int j = n_done; j < n_issued; ++j) {
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(bars + (j % S) * 8, (j / S) & 1) && global_ns() - t0 < 10000000ull) {
+            }
+        }
+    }
 }
 
 template <int D, int S, int NH>
@@ -557,7 +665,18 @@ extern "C" pa_status pa_paged_decode_attn(const void *q, int batch, int n_q_head
         !aligned4(req_pool_indices) || !aligned4(seq_lens))
         return PA_ERR_ALIGN;
 
-    DecodeArgs a{};
+    if ((int64_t)s.n_layers * s.size >= (int64_t)INT32_MAX - 16) return PA_ERR_SHAPE;
+    DecodeArgs a;
+    memset(&a, 0, sizeof a);
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)s.n_kv_heads * s.head_dim, (cuuint64_t)s.n_layers * s.size};
+        const cuuint64_t strides[1] = {(cuuint64_t)s.n_kv_heads * s.head_dim * 2};
+        const cuuint32_t box[2] = {64, kDecTile};
+        if (!encode_tmap_bf16(&a.tm_k, k_buf, 2, dims, strides, box) ||
+            !encode_tmap_bf16(&a.tm_v, v_buf, 2, dims, strides, box))
+            return PA_ERR_CUDA;
+    }
+    a.layer_row0 = layer_id * s.size;
     const int64_t layer_off = (int64_t)layer_id * s.size * s.n_kv_heads * s.head_dim;
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.k_layer = static_cast<const __nv_bfloat16 *>(k_buf) + layer_off;

@@ -67,6 +67,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// gpu-scope atomic add with release semantics (prior writes, including those
+// ordered before it by a CTA barrier, are visible before the add)
+__device__ __forceinline__ int atom_add_release_gpu(int *p, int v)
+{
+    int old;
+    asm volatile("atom.add.release.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1, uint32_t bar)
 {
