@@ -8,27 +8,28 @@
 // 0 .. p_r + i of the request, K/V rows read through req_to_token.
 //
 // How (persistent, one CTA per SM, warp-specialised, 320 threads):
-//  * Work item = (request, q-tile, kv head).  A q-tile packs the G query heads
-//    of one kv head into the MMA's M = 128 rows: 128/G consecutive tokens x G
-//    heads (token-major), so each K/V tile fetched serves all G heads.
-//  * warp 8 (producer): TMA.  Q tile via a 3-D tensor map (d, head, token);
+//  * Work item = (request, pair of q tiles, kv head).  A q tile packs the G
+//    query heads of one kv head into the MMA's M = 128 rows: 128/G
+//    consecutive tokens x G heads (token-major).  The two tiles A and B of a
+//    pair are consecutive and share every K/V tile the CTA fetches.
+//  * warp 8 (producer): TMA.  Q tiles via a 3-D tensor map (d, head, token);
 //    K/V tiles of 128 positions gathered through req_to_token: a group of 16
 //    positions on 16 consecutive slots (one page) is one 16-row box per 64-wide
-//    half, anything else falls back to 1-row boxes; positions past the item's
+//    half, anything else falls back to 1-row boxes; positions past the pair's
 //    last visible key load zeros (out-of-range rows).  128-byte swizzle, the
 //    layout the UMMA descriptors below expect.  Two K and two V stages.
-//  * warp 9 (MMA issuer, one thread): S = Q K^T into one of two TMEM buffers
-//    (128 lanes x 128 fp32 columns), O += P V into a third; commits signal the
-//    other warps.  S(t+1) is issued before PV(t) so the tensor core works on
-//    the next scores while the softmax warps finish the current tile.
-//  * warps 0-7 (softmax + epilogue): row i = TMEM lane i, warpgroup h owns
-//    columns [64h, 64h+64) of S, O and P; the two halves of a row exchange
-//    their maxima (and at the end their sums) through shared memory.  Causal
-//    mask (bottom-right aligned) only on diagonal tiles, online softmax in the
-//    log2 domain with a lazy running max (O in TMEM is rescaled only when the
-//    max grows by more than 2^8), P rounded to bf16 into shared memory as the
-//    A operand of the PV MMA.  Epilogue: O / l to bf16, rows of padding tokens
-//    are not written.
+//  * warp 9 (MMA issuer, one thread), tensor memory S_A | S_B | O_A | O_B
+//    (128 fp32 columns each):  S_X = Q_X K^T, then O_X += P_X V with P_X read
+//    from tensor memory, where the softmax left it over S_X (bf16 pairs).  The
+//    order S_A(t), S_B(t), PV_A(t), S_A(t+1), PV_B(t), S_B(t+1), ... gives each
+//    softmax warpgroup two MMA groups' time for its tile while the tensor core
+//    works on the other tile (ping-pong).
+//  * warps 0-3 own tile A's rows, warps 4-7 tile B's (row i = TMEM lane i):
+//    read S with tcgen05.ld, causal mask (bottom-right aligned) on diagonal
+//    tiles only, online softmax in the log2 domain with a lazy running max (O
+//    is rescaled in tensor memory only when the max grows by more than 2^8),
+//    P rounded to bf16 and stored back with tcgen05.st.  Epilogue: O / l to
+//    bf16, rows of padding tokens are not written.
 //  * Every mbarrier wait is bounded in time; on a time-out the CTA raises an
 //    abort flag, sets PA_DEVERR_TIMEOUT and unwinds, freeing its TMEM.
 #include <cuda.h>
@@ -40,27 +41,25 @@
 namespace pa {
 using namespace sm100;
 
-constexpr int kPfRows = 128;           // MMA M: rows of a q tile
-constexpr int kPfKeys = 128;           // keys per kv tile
-constexpr int kPfD = 128;              // head dim
-constexpr int kPfSoftmaxThreads = 256;  // warps 0-7: two warpgroups, one per 64-column half
-constexpr int kPfThreads = 320;         // + warp 8 (TMA producer) + warp 9 (MMA issuer)
+constexpr int kPfRows = 128;            // MMA M: rows of a q tile
+constexpr int kPfKeys = 128;            // keys per kv tile
+constexpr int kPfD = 128;               // head dim
+constexpr int kPfThreads = 320;         // 8 softmax warps + producer + MMA issuer
 constexpr int kWarpProducer = 8, kWarpMma = 9;
 constexpr int kPfMaxReqs = 2048;
-constexpr int kHalf = 128 * 128;       // one 128-row x 128-byte swizzled half tile (16 KB)
-constexpr int kOffQ = 0;               // 2 halves
-constexpr int kOffK = 2 * kHalf;       // 2 stages x 2 halves
-constexpr int kOffV = 6 * kHalf;       // 2 stages x 2 halves
-constexpr int kOffP = 10 * kHalf;      // 2 halves
+constexpr int kHalf = 128 * 128;        // one 128-row x 128-byte swizzled half tile (16 KB)
+constexpr int kOffQA = 0;               // 2 halves
+constexpr int kOffQB = 2 * kHalf;       // 2 halves
+constexpr int kOffK = 4 * kHalf;        // 2 stages x 2 halves
+constexpr int kOffV = 8 * kHalf;        // 2 stages x 2 halves
 constexpr int kOffBar = 12 * kHalf;
 enum { Q_FULL, Q_EMPTY, K_FULL, K_FULL1, K_EMPTY, K_EMPTY1, V_FULL, V_FULL1, V_EMPTY, V_EMPTY1,
-       S_FULL, S_FULL1, S_EMPTY, S_EMPTY1, P_FULL, O_DONE, O_EMPTY, XCH0, XCH1, XCH2, XCH3, N_BARS };
+       SA_FULL, SB_FULL, PA_FULL, PB_FULL, OA_FINAL, OB_FINAL, OA_EMPTY, OB_EMPTY, N_BARS };
 constexpr int kOffMisc = kOffBar + 32 * 8;
-constexpr int kOffXch = kOffMisc + 64;            // row max / sum exchange between the two halves
-constexpr int kOffPref = kOffXch + 3 * 128 * 4 * 2;
-constexpr uint32_t kTmemCols = 512;    // S0 | S1 | O | unused
+constexpr int kOffPref = kOffMisc + 64;
+constexpr uint32_t kTmemCols = 512;     // S_A | S_B | O_A | O_B
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);   // Q (K-major) x K (K-major)
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (K-major) x V (MN-major)
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (tensor memory) x V (MN-major)
 
 struct PrefillParams {
     CUtensorMap tm_q;     // 3-D (d, head, token) over q [T, Hq, 128]
@@ -80,7 +79,7 @@ struct PrefillParams {
 };
 
 struct PfItem {
-    int h, qs, q0, nq, p, row, n_keys, ntiles;
+    int h, qs, q0, nqa, nqb, p, row, n_keys, ntiles;   // q0: first token of tile A; nqb == 0: no tile B
 };
 
 __device__ __forceinline__ float ex2f(float x)
@@ -99,19 +98,20 @@ __device__ __forceinline__ PfItem pf_item(const PrefillParams &p, const int *s_p
     }
     const int r = lo;
     const int local = item - s_pref[r];
-    const int tiles_r = (s_pref[r + 1] - s_pref[r]) / p.Hkv;
+    const int pairs_r = (s_pref[r + 1] - s_pref[r]) / p.Hkv;
     const int jj = local / p.Hkv;
     PfItem I;
     I.h = local - jj * p.Hkv;
-    const int j = tiles_r - 1 - jj;            // later (heavier) q tiles first
+    const int jp = pairs_r - 1 - jj;            // later (heavier) pairs first
     I.qs = __ldg(p.qo_indptr + r);
     const int n_r = __ldg(p.qo_indptr + r + 1) - I.qs;
     const int L_r = __ldg(p.kv_indptr + r + 1) - __ldg(p.kv_indptr + r);
     I.p = L_r - n_r;
-    I.q0 = j * p.TQ;
-    I.nq = min(p.TQ, n_r - I.q0);
+    I.q0 = 2 * jp * p.TQ;
+    I.nqa = min(p.TQ, n_r - I.q0);
+    I.nqb = max(0, min(p.TQ, n_r - I.q0 - p.TQ));
     I.row = __ldg(p.req_pool_indices + r);
-    I.n_keys = I.p + I.q0 + I.nq;
+    I.n_keys = I.p + I.q0 + I.nqa + I.nqb;
     I.ntiles = (I.n_keys + kPfKeys - 1) / kPfKeys;
     return I;
 }
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     unsigned char *sb = smem_raw + (base - raw);
-    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP;
+    const uint32_t sQA = base + kOffQA, sQB = base + kOffQB, sK = base + kOffK, sV = base + kOffV;
     volatile int *s_abort = reinterpret_cast<volatile int *>(sb + kOffMisc);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sb + kOffMisc + 4);
     int *s_wsum = reinterpret_cast<int *>(sb + kOffMisc + 8);    // one int per warp
@@ -135,10 +135,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     if (tid == 0) {
         *s_abort = 0;
         for (int i = 0; i < N_BARS; ++i) {
-            const uint32_t cnt = (i == S_EMPTY || i == S_EMPTY1 || i == P_FULL || i == O_EMPTY)
-                                     ? (uint32_t)kPfSoftmaxThreads
-                                     : (i >= XCH0 ? 64u : 1u);
-            mbar_init(bar(i), cnt);
+            const bool softmax_arrive = i == PA_FULL || i == PB_FULL || i == OA_EMPTY || i == OB_EMPTY;
+            mbar_init(bar(i), softmax_arrive ? 128u : 1u);
         }
         fence_mbar_init();
     }
@@ -152,12 +150,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     }
 
     // ---------------------------------------------------------- planning
-    // q tiles per request (0 for an invalid request), exclusive prefix of
-    // tiles * Hkv; every thread scans a contiguous run of requests
+    // q-tile pairs per request (0 for an invalid request), exclusive prefix of
+    // pairs * Hkv; every thread scans a contiguous run of requests
     {
         const int per = (p.R + kPfThreads - 1) / kPfThreads;
         const int r_lo = min(p.R, tid * per), r_hi = min(p.R, r_lo + per);
-        auto tiles_of = [&](int r) -> int {
+        auto pairs_of = [&](int r) -> int {
             const int qa = __ldg(p.qo_indptr + r), qb = __ldg(p.qo_indptr + r + 1);
             const int n_r = qb - qa;
             const int L_r = __ldg(p.kv_indptr + r + 1) - __ldg(p.kv_indptr + r);
@@ -174,10 +172,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 set_error(err, PA_DEVERR_ROW);
                 return 0;
             }
-            return (n_r + p.TQ - 1) / p.TQ;
+            return (n_r + 2 * p.TQ - 1) / (2 * p.TQ);
         };
         int run = 0;
-        for (int r = r_lo; r < r_hi; ++r) run += tiles_of(r) * p.Hkv;
+        for (int r = r_lo; r < r_hi; ++r) run += pairs_of(r) * p.Hkv;
         int incl = run;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -191,7 +189,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         int excl = wbase + incl - run;
         for (int r = r_lo; r < r_hi; ++r) {
             s_pref[r] = excl;
-            excl += tiles_of(r) * p.Hkv;
+            excl += pairs_of(r) * p.Hkv;
         }
         if (tid == kPfThreads - 1) s_pref[p.R] = wbase + incl;
     }
@@ -209,9 +207,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
             const PfItem I = pf_item(p, s_pref, item);
             if (it > 0 && !mbar_wait(bar(Q_EMPTY), (it - 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar(Q_FULL), 2 * kHalf);
-                tma_load_3d(sQ, &p.tm_q, 0, I.h * G, I.qs + I.q0, bar(Q_FULL));
-                tma_load_3d(sQ + kHalf, &p.tm_q, 64, I.h * G, I.qs + I.q0, bar(Q_FULL));
+                mbar_arrive_expect_tx(bar(Q_FULL), 4 * kHalf);
+                tma_load_3d(sQA, &p.tm_q, 0, I.h * G, I.qs + I.q0, bar(Q_FULL));
+                tma_load_3d(sQA + kHalf, &p.tm_q, 64, I.h * G, I.qs + I.q0, bar(Q_FULL));
+                tma_load_3d(sQB, &p.tm_q, 0, I.h * G, I.qs + I.q0 + p.TQ, bar(Q_FULL));
+                tma_load_3d(sQB + kHalf, &p.tm_q, 64, I.h * G, I.qs + I.q0 + p.TQ, bar(Q_FULL));
             }
             const int32_t *r2t = p.req_to_token + (int64_t)I.row * p.max_ctx;
             const int col0 = I.h * kPfD;
@@ -277,126 +277,143 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     } else if (warp == kWarpMma) {
         // ================================================== MMA issuer
         if (lane == 0) {
-            int kt = 0, it = 0;
-            int pend_kt = -1, pend_it = 0;
-            bool pend_first = false, ok = true;
-            auto issue_pv = [&](int pkt, bool first, int pit) -> bool {
-                const int st = pkt & 1;
-                if (!mbar_wait(bar(P_FULL), pkt & 1, s_abort, err, PA_DEVERR_TIMEOUT)) return false;
-                if (!mbar_wait(bar(V_FULL + st), (pkt >> 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) return false;
-                if (first && pit > 0 && !mbar_wait(bar(O_EMPTY), (pit - 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT))
+            int kt = 0, ia = 0, ib = 0, ta = 0, tb = 0;   // tiles / items seen by tile A and B
+            bool ok = true;
+            auto wait = [&](int b, int ph) -> bool {
+                if (!mbar_wait(bar(b), ph & 1, s_abort, err, PA_DEVERR_TIMEOUT)) {
+                    ok = false;
                     return false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-                    const uint64_t a = smem_desc_sw128(sP + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(sV + st * 2 * kHalf + kk * 2048, kHalf, 1024);
-                    umma_ss(tmem + 256, a, b, kIdescPV, (kk > 0 || !first) ? 1u : 0u);
                 }
-                umma_commit(bar(V_EMPTY + st));
-                umma_commit(bar(O_DONE));
                 return true;
             };
-            for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x, ++it) {
-                const PfItem I = pf_item(p, s_pref, item);
-                if (!mbar_wait(bar(Q_FULL), it & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
-                for (int t = 0; t < I.ntiles; ++t, ++kt) {
-                    const int st = kt & 1;
-                    if (!mbar_wait(bar(K_FULL + st), (kt >> 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT) ||
-                        (kt >= 2 &&
-                         !mbar_wait(bar(S_EMPTY + st), ((kt >> 1) - 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+            auto qk = [&](uint32_t sQ, int st, uint32_t d_col) {
 #pragma unroll
-                    for (int kk = 0; kk < kPfD / 16; ++kk) {
-                        const uint64_t a = smem_desc_sw128(sQ + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-                        const uint64_t b =
-                            smem_desc_sw128(sK + st * 2 * kHalf + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-                        umma_ss(tmem + st * 128, a, b, kIdescS, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(bar(K_EMPTY + st));
-                    umma_commit(bar(S_FULL + st));
-                    if (t == I.ntiles - 1) umma_commit(bar(Q_EMPTY));
-                    if (pend_kt >= 0 && !issue_pv(pend_kt, pend_first, pend_it)) {
-                        ok = false;
-                        break;
-                    }
-                    pend_kt = kt;
-                    pend_first = (t == 0);
-                    pend_it = it;
+                for (int kk = 0; kk < kPfD / 16; ++kk) {
+                    const uint64_t a = smem_desc_sw128(sQ + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(sK + st * 2 * kHalf + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+                    umma_ss(tmem + d_col, a, b, kIdescS, kk > 0 ? 1u : 0u);
                 }
+            };
+            auto pv = [&](uint32_t p_col, uint32_t o_col, int st, bool first) {
+#pragma unroll
+                for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+                    const uint64_t b = smem_desc_sw128(sV + st * 2 * kHalf + kk * 2048, kHalf, 1024);
+                    umma_ts(tmem + o_col, tmem + p_col + kk * 8, b, kIdescPV, (kk > 0 || !first) ? 1u : 0u);
+                }
+            };
+            for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
+                const PfItem I = pf_item(p, s_pref, item);
+                const bool hasB = I.nqb > 0;
+                const int it = ia;   // items so far (every item has a tile A)
+                if (!wait(Q_FULL, it)) break;
+                // S_A(0), S_B(0)
+                if (!wait(K_FULL + (kt & 1), kt >> 1)) break;
+                tc_fence_after();
+                qk(sQA, kt & 1, 0);
+                umma_commit(bar(SA_FULL));
+                if (hasB) {
+                    qk(sQB, kt & 1, 128);
+                    umma_commit(bar(SB_FULL));
+                }
+                umma_commit(bar(K_EMPTY + (kt & 1)));
+                for (int t = 0; t < I.ntiles; ++t, ++kt) {
+                    const int st = kt & 1, st1 = (kt + 1) & 1;
+                    const bool more = t + 1 < I.ntiles;
+                    // PV_A(t)
+                    if (!wait(PA_FULL, ta) || !wait(V_FULL + st, kt >> 1)) break;
+                    if (t == 0 && ia > 0 && !wait(OA_EMPTY, ia - 1)) break;
+                    tc_fence_after();
+                    pv(0, 256, st, t == 0);
+                    ++ta;
+                    if (!more) umma_commit(bar(OA_FINAL));
+                    // S_A(t+1)
+                    if (more) {
+                        if (!wait(K_FULL + st1, (kt + 1) >> 1)) break;
+                        tc_fence_after();
+                        qk(sQA, st1, 0);
+                        umma_commit(bar(SA_FULL));
+                    }
+                    // PV_B(t)
+                    if (hasB) {
+                        if (!wait(PB_FULL, tb)) break;
+                        if (t == 0 && ib > 0 && !wait(OB_EMPTY, ib - 1)) break;
+                        tc_fence_after();
+                        pv(128, 384, st, t == 0);
+                        ++tb;
+                        if (!more) umma_commit(bar(OB_FINAL));
+                    }
+                    umma_commit(bar(V_EMPTY + st));
+                    // S_B(t+1)
+                    if (more) {
+                        if (hasB) {
+                            qk(sQB, st1, 128);
+                            umma_commit(bar(SB_FULL));
+                        }
+                        umma_commit(bar(K_EMPTY + st1));
+                    } else {
+                        umma_commit(bar(Q_EMPTY));
+                    }
+                }
+                ++ia;
+                if (hasB) ++ib;
             }
-            if (ok && pend_kt >= 0) issue_pv(pend_kt, pend_first, pend_it);
         }
         __syncwarp();
     } else {
-        // ============================ softmax + epilogue (row, column half)
-        // thread -> row (TMEM lane) and one 64-column half of S, O and P
-        const int half = warp >> 2;
-        const int row = tid & 127;
+        // ======================= softmax + epilogue: warpgroup X owns tile X
+        const int X = warp >> 2;                  // 0: tile A, 1: tile B
+        const int row = tid & 127;                // TMEM lane = row of the tile
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t o_addr = tmem + lane_base + 256 + half * 64;
-        float *xmax = reinterpret_cast<float *>(sb + kOffXch);     // [parity][half][row]
-        float *xsum = xmax + 4 * 128;                              // [half][row]
-        const uint32_t xbar = bar(XCH0 + (warp & 3));
-        uint32_t xph = 0;
+        const uint32_t s_addr = tmem + lane_base + X * 128;     // S_X, later P_X (bf16 pairs)
+        const uint32_t o_addr = tmem + lane_base + 256 + X * 128;
+        const int b_s_full = X ? SB_FULL : SA_FULL, b_p_full = X ? PB_FULL : PA_FULL;
+        const int b_o_final = X ? OB_FINAL : OA_FINAL, b_o_empty = X ? OB_EMPTY : OA_EMPTY;
         const float sl2 = p.scale_log2;
-        int kt = 0;
+        int tx = 0, ix = 0;       // tiles and items this warpgroup has processed
         bool ok = true;
         for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
             const PfItem I = pf_item(p, s_pref, item);
-            const int tok = row / G;                    // token of this row within the q tile
-            const int qpos = I.p + I.q0 + tok;           // its position in the request
+            const int nq = X ? I.nqb : I.nqa;
+            if (nq <= 0) continue;                // no tile B in this pair
+            const int q0 = I.q0 + X * p.TQ;
+            const int tok = row / G;              // token of this row within the tile
+            const int qpos = I.p + q0 + tok;      // its position in the request
             float m_run = -INFINITY, l_run = 0.f;
-            for (int t = 0; t < I.ntiles; ++t, ++kt) {
-                const int st = kt & 1;
-                if (!mbar_wait(bar(S_FULL + st), (kt >> 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) {
+            for (int t = 0; t < I.ntiles; ++t, ++tx) {
+                if (!mbar_wait(bar(b_s_full), tx & 1, s_abort, err, PA_DEVERR_TIMEOUT)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t r[64];
-                {
-                    uint32_t (&r0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
-                    uint32_t (&r1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
-                    const uint32_t s_addr = tmem + lane_base + st * 128 + half * 64;
-                    tmem_ld32(s_addr, r0);
-                    tmem_ld32(s_addr + 32, r1);
-                    tmem_wait_ld();
-                }
-                const int limit = qpos - t * kPfKeys - half * 64;    // columns <= limit are visible
+                const int limit = qpos - t * kPfKeys;    // columns <= limit are visible
+                // row maximum, 64 columns at a time
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-                if (limit >= 63) {
 #pragma unroll
-                    for (int c = 0; c < 64; c += 4) {
-                        mx0 = fmaxf(mx0, __uint_as_float(r[c]));
-                        mx1 = fmaxf(mx1, __uint_as_float(r[c + 1]));
-                        mx2 = fmaxf(mx2, __uint_as_float(r[c + 2]));
-                        mx3 = fmaxf(mx3, __uint_as_float(r[c + 3]));
-                    }
-                } else {
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[64];
+                    tmem_ld32(s_addr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    tmem_ld32(s_addr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_wait_ld();
+                    if (limit >= hh * 64 + 63) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const float v = c <= limit ? __uint_as_float(r[c]) : -INFINITY;
-                        r[c] = __float_as_uint(v);
-                        if ((c & 3) == 0) mx0 = fmaxf(mx0, v);
-                        if ((c & 3) == 1) mx1 = fmaxf(mx1, v);
-                        if ((c & 3) == 2) mx2 = fmaxf(mx2, v);
-                        if ((c & 3) == 3) mx3 = fmaxf(mx3, v);
+                        for (int c = 0; c < 64; c += 4) {
+                            mx0 = fmaxf(mx0, __uint_as_float(r[c]));
+                            mx1 = fmaxf(mx1, __uint_as_float(r[c + 1]));
+                            mx2 = fmaxf(mx2, __uint_as_float(r[c + 2]));
+                            mx3 = fmaxf(mx3, __uint_as_float(r[c + 3]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; c += 4) {
+                            const int cc = hh * 64 + c;
+                            mx0 = fmaxf(mx0, cc <= limit ? __uint_as_float(r[c]) : -INFINITY);
+                            mx1 = fmaxf(mx1, cc + 1 <= limit ? __uint_as_float(r[c + 1]) : -INFINITY);
+                            mx2 = fmaxf(mx2, cc + 2 <= limit ? __uint_as_float(r[c + 2]) : -INFINITY);
+                            mx3 = fmaxf(mx3, cc + 3 <= limit ? __uint_as_float(r[c + 3]) : -INFINITY);
+                        }
                     }
                 }
-                float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-                // row maximum across the two halves
-                xmax[((kt & 1) * 2 + half) * 128 + row] = mx;
-                mbar_arrive(xbar);
-                if (!mbar_wait(xbar, xph & 1, s_abort, err, PA_DEVERR_TIMEOUT)) {
-                    ok = false;
-                    break;
-                }
-                ++xph;
-                mx = fmaxf(mx, xmax[((kt & 1) * 2 + (half ^ 1)) * 128 + row]);
+                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
                 float m_new = m_run;
                 bool rescale = false;
                 if (mx > m_run && (m_run == -INFINITY || (mx - m_run) * sl2 > 8.f)) {
@@ -406,28 +423,43 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 const float alpha = rescale ? ex2f((m_run - m_new) * sl2) : 1.f;
                 m_run = m_new;
                 const float mb = m_new == -INFINITY ? 0.f : m_new * sl2;
-                uint32_t pk[32];
+                // P = exp2(s*scale - m): 64 columns at a time, written back as
+                // bf16 pairs over the first 64 columns of S_X (already consumed)
                 float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    const float v0 = ex2f(fmaf(__uint_as_float(r[c]), sl2, -mb));
-                    const float v1 = ex2f(fmaf(__uint_as_float(r[c + 1]), sl2, -mb));
-                    sum0 += v0;
-                    sum1 += v1;
-                    pk[c / 2] = pack_bf16x2(v0, v1);
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t r[64];
+                    tmem_ld32(s_addr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    tmem_ld32(s_addr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_wait_ld();
+                    uint32_t pk[32];
+                    if (limit >= hh * 64 + 63) {
+#pragma unroll
+                        for (int c = 0; c < 64; c += 2) {
+                            const float v0 = ex2f(fmaf(__uint_as_float(r[c]), sl2, -mb));
+                            const float v1 = ex2f(fmaf(__uint_as_float(r[c + 1]), sl2, -mb));
+                            sum0 += v0;
+                            sum1 += v1;
+                            pk[c / 2] = pack_bf16x2(v0, v1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; c += 2) {
+                            const int cc = hh * 64 + c;
+                            const float v0 = cc <= limit ? ex2f(fmaf(__uint_as_float(r[c]), sl2, -mb)) : 0.f;
+                            const float v1 = cc + 1 <= limit ? ex2f(fmaf(__uint_as_float(r[c + 1]), sl2, -mb)) : 0.f;
+                            sum0 += v0;
+                            sum1 += v1;
+                            pk[c / 2] = pack_bf16x2(v0, v1);
+                        }
+                    }
+                    tmem_st32(s_addr + hh * 32, pk);
                 }
                 l_run = l_run * alpha + (sum0 + sum1);
-                tc_fence_before();
-                mbar_arrive(bar(S_EMPTY + st));
-                // the previous PV must be done: P's buffer is free and O is stable
-                if (kt > 0 && !mbar_wait(bar(O_DONE), (kt - 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                // O_X is stable here: S_X(t) completing implies PV_X(t-1) completed
                 if (t > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                    for (int ch = 0; ch < 2; ++ch) {
+                    for (int ch = 0; ch < 4; ++ch) {
                         uint32_t o[32];
                         tmem_ld32(o_addr + ch * 32, o);
                         tmem_wait_ld();
@@ -435,33 +467,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                         for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
                         tmem_st32(o_addr + ch * 32, o);
                     }
-                    tmem_wait_st();
                 }
-                // P: this half's 64 keys of the row -> its K-major 128-byte swizzled region
-                unsigned char *prow = sb + kOffP + half * kHalf + row * 128;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(prow + ((c ^ (row & 7)) << 4)) =
-                        make_uint4(pk[c * 4], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
-                fence_proxy_async_smem();
+                tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(P_FULL));
+                mbar_arrive(bar(b_p_full));
             }
             if (!ok) break;
             // ------------------------------------------------ epilogue
-            if (!mbar_wait(bar(O_DONE), (kt - 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
+            if (!mbar_wait(bar(b_o_final), ix & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
             tc_fence_after();
-            xsum[half * 128 + row] = l_run;
-            mbar_arrive(xbar);
-            if (!mbar_wait(xbar, xph & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
-            ++xph;
-            const float l_tot = l_run + xsum[(half ^ 1) * 128 + row];
-            const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-            const bool row_ok = tok < I.nq;
-            __nv_bfloat16 *dst =
-                p.out + ((int64_t)(I.qs + I.q0 + tok) * p.Hq + I.h * G + (row - tok * G)) * kPfD + half * 64;
+            const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+            const bool row_ok = tok < nq;
+            __nv_bfloat16 *dst = p.out + ((int64_t)(I.qs + q0 + tok) * p.Hq + I.h * G + (row - tok * G)) * kPfD;
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
+            for (int ch = 0; ch < 4; ++ch) {
                 uint32_t o[32];
                 tmem_ld32(o_addr + ch * 32, o);
                 tmem_wait_ld();
@@ -478,7 +497,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(O_EMPTY));
+            mbar_arrive(bar(b_o_empty));
+            ++ix;
         }
     }
 
@@ -487,13 +507,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-}
-
-// ------------------------------------------------------------------ host
-static bool encode(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                   const cuuint32_t *box)
-{
-    return encode_tmap_bf16(m, ptr, rank, dims, strides, box);
 }
 
 }  // namespace pa
@@ -532,14 +545,16 @@ extern "C" pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_
         const cuuint64_t dims[3] = {(cuuint64_t)kPfD, (cuuint64_t)n_q_heads, (cuuint64_t)n_tokens};
         const cuuint64_t strides[2] = {(cuuint64_t)kPfD * 2, (cuuint64_t)n_q_heads * kPfD * 2};
         const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
-        if (!encode(&prm.tm_q, q, 3, dims, strides, box)) return PA_ERR_CUDA;
+        if (!encode_tmap_bf16(&prm.tm_q, q, 3, dims, strides, box)) return PA_ERR_CUDA;
     }
     {
         const cuuint64_t dims[2] = {(cuuint64_t)s.n_kv_heads * kPfD, (cuuint64_t)s.n_layers * s.size};
         const cuuint64_t strides[1] = {(cuuint64_t)s.n_kv_heads * kPfD * 2};
         const cuuint32_t box16[2] = {64, 16}, box1[2] = {64, 1};
-        if (!encode(&prm.tm_k16, k_buf, 2, dims, strides, box16) || !encode(&prm.tm_k1, k_buf, 2, dims, strides, box1) ||
-            !encode(&prm.tm_v16, v_buf, 2, dims, strides, box16) || !encode(&prm.tm_v1, v_buf, 2, dims, strides, box1))
+        if (!encode_tmap_bf16(&prm.tm_k16, k_buf, 2, dims, strides, box16) ||
+            !encode_tmap_bf16(&prm.tm_k1, k_buf, 2, dims, strides, box1) ||
+            !encode_tmap_bf16(&prm.tm_v16, v_buf, 2, dims, strides, box16) ||
+            !encode_tmap_bf16(&prm.tm_v1, v_buf, 2, dims, strides, box1))
             return PA_ERR_CUDA;
     }
     prm.qo_indptr = qo_indptr;
