@@ -316,6 +316,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                     umma_commit(bar(SB_FULL));
                 }
                 umma_commit(bar(K_EMPTY + (kt & 1)));
+                if (I.ntiles == 1) umma_commit(bar(Q_EMPTY));   // the item's last QK^T: Q may be refilled
                 for (int t = 0; t < I.ntiles; ++t, ++kt) {
                     const int st = kt & 1, st1 = (kt + 1) & 1;
                     const bool more = t + 1 < I.ntiles;
@@ -350,8 +351,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                             umma_commit(bar(SB_FULL));
                         }
                         umma_commit(bar(K_EMPTY + st1));
-                    } else {
-                        umma_commit(bar(Q_EMPTY));
+                        if (t + 2 == I.ntiles) umma_commit(bar(Q_EMPTY));   // last QK^T of the item issued
                     }
                 }
                 ++ia;
