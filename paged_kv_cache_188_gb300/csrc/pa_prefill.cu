@@ -386,32 +386,25 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 }
                 tc_fence_after();
                 const int limit = qpos - t * kPfKeys;    // columns <= limit are visible
-                // row maximum, 64 columns at a time
+                // the whole row of S in registers: four loads, one wait
+                uint32_t r[128];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    tmem_ld32(s_addr + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[ch * 32]));
+                tmem_wait_ld();
+                const bool diag = limit < kPfKeys - 1;
+                if (diag) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c > limit) r[c] = __float_as_uint(-INFINITY);
+                }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[64];
-                    tmem_ld32(s_addr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    tmem_ld32(s_addr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                    tmem_wait_ld();
-                    if (limit >= hh * 64 + 63) {
-#pragma unroll
-                        for (int c = 0; c < 64; c += 4) {
-                            mx0 = fmaxf(mx0, __uint_as_float(r[c]));
-                            mx1 = fmaxf(mx1, __uint_as_float(r[c + 1]));
-                            mx2 = fmaxf(mx2, __uint_as_float(r[c + 2]));
-                            mx3 = fmaxf(mx3, __uint_as_float(r[c + 3]));
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 64; c += 4) {
-                            const int cc = hh * 64 + c;
-                            mx0 = fmaxf(mx0, cc <= limit ? __uint_as_float(r[c]) : -INFINITY);
-                            mx1 = fmaxf(mx1, cc + 1 <= limit ? __uint_as_float(r[c + 1]) : -INFINITY);
-                            mx2 = fmaxf(mx2, cc + 2 <= limit ? __uint_as_float(r[c + 2]) : -INFINITY);
-                            mx3 = fmaxf(mx3, cc + 3 <= limit ? __uint_as_float(r[c + 3]) : -INFINITY);
-                        }
-                    }
+                for (int c = 0; c < 128; c += 4) {
+                    mx0 = fmaxf(mx0, __uint_as_float(r[c]));
+                    mx1 = fmaxf(mx1, __uint_as_float(r[c + 1]));
+                    mx2 = fmaxf(mx2, __uint_as_float(r[c + 2]));
+                    mx3 = fmaxf(mx3, __uint_as_float(r[c + 3]));
                 }
                 const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
                 float m_new = m_run;
@@ -423,35 +416,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 const float alpha = rescale ? ex2f((m_run - m_new) * sl2) : 1.f;
                 m_run = m_new;
                 const float mb = m_new == -INFINITY ? 0.f : m_new * sl2;
-                // P = exp2(s*scale - m): 64 columns at a time, written back as
-                // bf16 pairs over the first 64 columns of S_X (already consumed)
+                // P = exp2(s*scale - m) (masked entries are -inf -> 0), written
+                // back as bf16 pairs over the first 64 columns of S_X
                 float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t r[64];
-                    tmem_ld32(s_addr + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    tmem_ld32(s_addr + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                    tmem_wait_ld();
                     uint32_t pk[32];
-                    if (limit >= hh * 64 + 63) {
 #pragma unroll
-                        for (int c = 0; c < 64; c += 2) {
-                            const float v0 = ex2f(fmaf(__uint_as_float(r[c]), sl2, -mb));
-                            const float v1 = ex2f(fmaf(__uint_as_float(r[c + 1]), sl2, -mb));
-                            sum0 += v0;
-                            sum1 += v1;
-                            pk[c / 2] = pack_bf16x2(v0, v1);
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 64; c += 2) {
-                            const int cc = hh * 64 + c;
-                            const float v0 = cc <= limit ? ex2f(fmaf(__uint_as_float(r[c]), sl2, -mb)) : 0.f;
-                            const float v1 = cc + 1 <= limit ? ex2f(fmaf(__uint_as_float(r[c + 1]), sl2, -mb)) : 0.f;
-                            sum0 += v0;
-                            sum1 += v1;
-                            pk[c / 2] = pack_bf16x2(v0, v1);
-                        }
+                    for (int c = 0; c < 64; c += 2) {
+                        const float v0 = ex2f(fmaf(__uint_as_float(r[hh * 64 + c]), sl2, -mb));
+                        const float v1 = ex2f(fmaf(__uint_as_float(r[hh * 64 + c + 1]), sl2, -mb));
+                        sum0 += v0;
+                        sum1 += v1;
+                        pk[c / 2] = pack_bf16x2(v0, v1);
                     }
                     tmem_st32(s_addr + hh * 32, pk);
                 }
