@@ -91,7 +91,11 @@ const char *pa_status_string(pa_status s);
 size_t pa_decode_workspace_bytes(int max_batch, int n_q_heads, int n_kv_heads, int head_dim,
                                  int max_splits);
 
-/* Prefill workspace: the error word plus a small fixed area. */
+/* Prefill workspace: the error word plus the prefill work queue, two int32
+ * words inside the 256-byte header (the next work item to claim and the number
+ * of CTAs that have finished; the kernel returns both to zero before it ends).
+ * A decode workspace also serves prefill.  A workspace serves one call at a
+ * time: calls that share one must be ordered on a stream. */
 size_t pa_prefill_workspace_bytes(void);
 
 /* Zero the whole workspace on `st` (cudaMemsetAsync).  Call once after

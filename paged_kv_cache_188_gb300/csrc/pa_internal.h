@@ -11,6 +11,10 @@
 namespace pa {
 
 constexpr int kWorkspaceHeader = 256;   // error word + padding at the start of a workspace
+// prefill work queue, int32 words inside the header (separate 64-byte sectors):
+// the next item to claim and the number of CTAs that have finished
+constexpr int kPrefillQueueWord = 16;
+constexpr int kPrefillDoneWord = 32;
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -12,6 +12,9 @@
 //    query heads of one kv head into the MMA's M = 128 rows: 128/G
 //    consecutive tokens x G heads (token-major).  The two tiles A and B of a
 //    pair are consecutive and share every K/V tile the CTA fetches.
+//  * Items are claimed from a counter in the workspace (heaviest pairs of a
+//    request first), so CTAs that drew short items take more of them; the
+//    producer hands each claim to the other roles through a small ring.
 //  * warp 8 (producer): TMA.  Q tiles via a 3-D tensor map (d, head, token);
 //    K/V tiles of 128 positions gathered through req_to_token: a group of 16
 //    positions on 16 consecutive slots (one page) is one 16-row box per 64-wide
@@ -53,10 +56,14 @@ constexpr int kOffQB = 2 * kHalf;       // 2 halves
 constexpr int kOffK = 4 * kHalf;        // 2 stages x 2 halves
 constexpr int kOffV = 8 * kHalf;        // 2 stages x 2 halves
 constexpr int kOffBar = 12 * kHalf;
+constexpr int kRing = 4;               // claimed work items handed from the producer to the other roles
 enum { Q_FULL, Q_EMPTY, K_FULL, K_FULL1, K_EMPTY, K_EMPTY1, V_FULL, V_FULL1, V_EMPTY, V_EMPTY1,
-       SA_FULL, SB_FULL, PA_FULL, PB_FULL, OA_FINAL, OB_FINAL, OA_EMPTY, OB_EMPTY, N_BARS };
+       SA_FULL, SB_FULL, PA_FULL, PB_FULL, OA_FINAL, OB_FINAL, OA_EMPTY, OB_EMPTY,
+       ITEM_FULL, ITEM_EMPTY = ITEM_FULL + kRing, N_BARS = ITEM_EMPTY + kRing };
+static_assert(N_BARS <= 32, "barrier area holds 32 barriers");
+constexpr int kItemReaders = 1 + 8;     // the MMA thread and the eight softmax warps
 constexpr int kOffMisc = kOffBar + 32 * 8;
-constexpr int kOffPref = kOffMisc + 64;
+constexpr int kOffPref = kOffMisc + 128;
 constexpr uint32_t kTmemCols = 512;     // S_A | S_B | O_A | O_B
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);   // Q (K-major) x K (K-major)
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (tensor memory) x V (MN-major)
@@ -73,6 +80,7 @@ struct PrefillParams {
     const int32_t *req_pool_indices;
     __nv_bfloat16 *out;
     int32_t *err;
+    int32_t *queue;       // [0]: next item to claim, [done]: CTAs finished (kept at 0 between launches)
     int T, Hq, Hkv, G, TQ, R;
     int size, layer_row0, total_rows, req_rows, max_ctx;
     float scale_log2;
@@ -126,6 +134,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     volatile int *s_abort = reinterpret_cast<volatile int *>(sb + kOffMisc);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sb + kOffMisc + 4);
     int *s_wsum = reinterpret_cast<int *>(sb + kOffMisc + 8);    // one int per warp
+    volatile int *s_item = reinterpret_cast<volatile int *>(sb + kOffMisc + 64);   // kRing claimed items
     int *s_pref = reinterpret_cast<int *>(sb + kOffPref);
     auto bar = [&](int i) -> uint32_t { return base + kOffBar + i * 8; };
 
@@ -136,7 +145,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         *s_abort = 0;
         for (int i = 0; i < N_BARS; ++i) {
             const bool softmax_arrive = i == PA_FULL || i == PB_FULL || i == OA_EMPTY || i == OB_EMPTY;
-            mbar_init(bar(i), softmax_arrive ? 128u : 1u);
+            const bool item_read = i >= ITEM_EMPTY && i < ITEM_EMPTY + kRing;
+            mbar_init(bar(i), softmax_arrive ? 128u : item_read ? (uint32_t)kItemReaders : 1u);
         }
         fence_mbar_init();
     }
@@ -201,9 +211,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
 
     if (warp == kWarpProducer) {
         // ================================================== TMA producer
-        int kt = 0, it = 0;
+        // Items are claimed one at a time from a global counter, so a CTA that
+        // drew short items takes more of them; each claim (and finally the
+        // first index past the end) goes to the other roles through a ring.
+        int kt = 0;
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x, ++it) {
+        for (int it = 0; ok; ++it) {
+            const int slot = it % kRing;
+            if (it >= kRing && !mbar_wait(bar(ITEM_EMPTY + slot), (it / kRing - 1) & 1, s_abort, err,
+                                          PA_DEVERR_TIMEOUT))
+                break;
+            int item = 0;
+            if (lane == 0) {
+                item = atomicAdd(p.queue, 1);
+                s_item[slot] = item;
+                mbar_arrive(bar(ITEM_FULL + slot));
+            }
+            item = __shfl_sync(0xffffffffu, item, 0);
+            if (item >= total_items) break;
             const PfItem I = pf_item(p, s_pref, item);
             if (it > 0 && !mbar_wait(bar(Q_EMPTY), (it - 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
             if (lane == 0) {
@@ -301,7 +326,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                     umma_ts(tmem + o_col, tmem + p_col + kk * 8, b, kIdescPV, (kk > 0 || !first) ? 1u : 0u);
                 }
             };
-            for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
+            for (int n = 0; ok; ++n) {
+                if (!wait(ITEM_FULL + n % kRing, n / kRing)) break;
+                const int item = s_item[n % kRing];
+                mbar_arrive(bar(ITEM_EMPTY + n % kRing));
+                if (item >= total_items) break;
                 const PfItem I = pf_item(p, s_pref, item);
                 const bool hasB = I.nqb > 0;
                 const int it = ia;   // items so far (every item has a tile A)
@@ -371,7 +400,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         const float sl2 = p.scale_log2;
         int tx = 0, ix = 0;       // tiles and items this warpgroup has processed
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < total_items; item += gridDim.x) {
+        for (int n = 0; ok; ++n) {
+            if (!mbar_wait(bar(ITEM_FULL + n % kRing), (n / kRing) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
+            const int item = s_item[n % kRing];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ITEM_EMPTY + n % kRing));
+            if (item >= total_items) break;
             const PfItem I = pf_item(p, s_pref, item);
             const int nq = X ? I.nqb : I.nqa;
             if (nq <= 0) continue;                // no tile B in this pair
@@ -484,6 +518,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    // the last CTA to finish returns the queue to zero for the next launch;
+    // every CTA's claims precede its increment here
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(p.queue + (kPrefillDoneWord - kPrefillQueueWord), 1) == (int)gridDim.x - 1) {
+            atomicExch(p.queue, 0);
+            atomicExch(p.queue + (kPrefillDoneWord - kPrefillQueueWord), 0);
+        }
+    }
 }
 
 }  // namespace pa
@@ -540,6 +583,7 @@ extern "C" pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_
     prm.req_pool_indices = req_pool_indices;
     prm.out = static_cast<__nv_bfloat16 *>(out);
     prm.err = static_cast<int32_t *>(workspace);
+    prm.queue = static_cast<int32_t *>(workspace) + kPrefillQueueWord;
     prm.T = n_tokens;
     prm.Hq = n_q_heads;
     prm.Hkv = s.n_kv_heads;

@@ -81,9 +81,14 @@ def test_deterministic_graph_replay_and_padding_rows_untouched():
     with torch.cuda.graph(g, stream=s):
         api.pa_paged_prefill_attn(pb.q, pb.kv.k_buf, pb.kv.v_buf, 0, pb.qo_indptr, pb.kv_indptr,
                                   pb.kv.req_to_token, pb.kv.req_pool_indices, pb.scale, ws, og, stream=s)
-    g.replay()
-    torch.cuda.synchronize()
-    assert torch.equal(out1.view(torch.int16), og.view(torch.int16))
+    for _ in range(3):
+        og.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out1.view(torch.int16), og.view(torch.int16))
+    # the work queue in the workspace header is back at zero after every launch
+    words = ws.view(torch.int32)
+    assert int(words[16]) == 0 and int(words[32]) == 0
     # a pack of one request writes only its own rows
     T = pb.q.shape[0]
     out = torch.full_like(pb.q, 7.0)
@@ -94,6 +99,7 @@ def test_deterministic_graph_replay_and_padding_rows_untouched():
     torch.cuda.synchronize()
     assert torch.equal(out[:77].view(torch.int16), out1[:77].view(torch.int16))
     assert (out[77:T] == 7.0).all()
+    assert int(words[16]) == 0 and int(words[32]) == 0
 
 
 def test_invalid_request_is_skipped_and_flagged():
