@@ -63,7 +63,9 @@ enum { Q_FULL, Q_EMPTY, K_FULL, K_FULL1, K_EMPTY, K_EMPTY1, V_FULL, V_FULL1, V_E
 static_assert(N_BARS <= 32, "barrier area holds 32 barriers");
 constexpr int kItemReaders = 1 + 8;     // the MMA thread and the eight softmax warps
 constexpr int kOffMisc = kOffBar + 32 * 8;
-constexpr int kOffPref = kOffMisc + 128;
+constexpr int kStageBytes = 32 * 64;    // per softmax warp: 32 rows x 32 bf16 of the output
+constexpr int kOffStage = kOffMisc + 128;
+constexpr int kOffPref = kOffStage + 8 * kStageBytes;
 constexpr uint32_t kTmemCols = 512;     // S_A | S_B | O_A | O_B
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);   // Q (K-major) x K (K-major)
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // P (tensor memory) x V (MN-major)
@@ -487,28 +489,44 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
             // ------------------------------------------------ epilogue
             if (!mbar_wait(bar(b_o_final), ix & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
             tc_fence_after();
+            uint32_t o[128];
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch)
+                tmem_ld32(o_addr + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&o[ch * 32]));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(b_o_empty));          // O_X is in registers: the next item may overwrite it
             const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-            const bool row_ok = tok < nq;
-            __nv_bfloat16 *dst = p.out + ((int64_t)(I.qs + q0 + tok) * p.Hq + I.h * G + (row - tok * G)) * kPfD;
+            uint32_t ob[64];                      // O / l as bf16 pairs
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+                ob[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
+            // 32 columns at a time through this warp's staging buffer (row
+            // lane, 16-byte chunks XOR-swizzled by row so neither side
+            // conflicts), then out with four lanes on 64 contiguous bytes
+            const uint32_t stg = base + kOffStage + warp * kStageBytes;
+            const int rr0 = lane >> 2, cc = lane & 3;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
-                uint32_t o[32];
-                tmem_ld32(o_addr + ch * 32, o);
-                tmem_wait_ld();
-                if (row_ok) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv_l, __uint_as_float(o[q * 8 + 1]) * inv_l);
-                        v.y = pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv_l, __uint_as_float(o[q * 8 + 3]) * inv_l);
-                        v.z = pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv_l, __uint_as_float(o[q * 8 + 5]) * inv_l);
-                        v.w = pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv_l, __uint_as_float(o[q * 8 + 7]) * inv_l);
-                        *reinterpret_cast<uint4 *>(dst + ch * 32 + q * 8) = v;
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t *v = &ob[ch * 16 + c * 4];
+                    st_shared_v4(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4), v[0], v[1], v[2], v[3]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = 8 * i + rr0;                 // staged row = tile row (warp & 3) * 32 + rr
+                    const uint4 v = ld_shared_v4(stg + rr * 64 + ((cc ^ ((rr >> 1) & 3)) << 4));
+                    const int trow = (warp & 3) * 32 + rr;
+                    const int ttok = trow / G;
+                    if (ttok < nq) {
+                        __nv_bfloat16 *dst = p.out + ((int64_t)(I.qs + q0 + ttok) * p.Hq + I.h * G + (trow - ttok * G)) * kPfD;
+                        *reinterpret_cast<uint4 *>(dst + ch * 32 + cc * 8) = v;
                     }
                 }
+                __syncwarp();
             }
-            tc_fence_before();
-            mbar_arrive(bar(b_o_empty));
             ++ix;
         }
     }
