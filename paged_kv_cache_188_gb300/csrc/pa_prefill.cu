@@ -61,10 +61,11 @@ enum { Q_FULL, Q_EMPTY, K_FULL, K_FULL1, K_EMPTY, K_EMPTY1, V_FULL, V_FULL1, V_E
        SA_FULL, SB_FULL, PA_FULL, PB_FULL, OA_FINAL, OB_FINAL, OA_EMPTY, OB_EMPTY,
        ITEM_FULL, ITEM_EMPTY = ITEM_FULL + kRing, N_BARS = ITEM_EMPTY + kRing };
 static_assert(N_BARS <= 32, "barrier area holds 32 barriers");
-constexpr int kItemReaders = 1 + 8;     // the MMA thread and the eight softmax warps
+constexpr int kItemReaders = 1 + 8;     // the MMA warp and the eight softmax warps
 constexpr int kOffMisc = kOffBar + 32 * 8;
+constexpr int kOffRing = kOffMisc + 64;   // kRing work-item descriptions
 constexpr int kStageBytes = 32 * 64;    // per softmax warp: 32 rows x 32 bf16 of the output
-constexpr int kOffStage = kOffMisc + 128;
+constexpr int kOffStage = kOffMisc + 256;
 constexpr int kOffPref = kOffStage + 8 * kStageBytes;
 constexpr uint32_t kTmemCols = 512;     // S_A | S_B | O_A | O_B
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);   // Q (K-major) x K (K-major)
@@ -88,9 +89,12 @@ struct PrefillParams {
     float scale_log2;
 };
 
-struct PfItem {
+struct alignas(16) PfItem {
     int h, qs, q0, nqa, nqb, p, row, n_keys, ntiles;   // q0: first token of tile A; nqb == 0: no tile B
+    int end;                                           // 1: no more items for this CTA
+    int pad[2];
 };
+static_assert(kOffRing + kRing * (int)sizeof(PfItem) <= kOffMisc + 256, "item ring fits the misc area");
 
 __device__ __forceinline__ float ex2f(float x)
 {
@@ -136,7 +140,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
     volatile int *s_abort = reinterpret_cast<volatile int *>(sb + kOffMisc);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sb + kOffMisc + 4);
     int *s_wsum = reinterpret_cast<int *>(sb + kOffMisc + 8);    // one int per warp
-    volatile int *s_item = reinterpret_cast<volatile int *>(sb + kOffMisc + 64);   // kRing claimed items
+    PfItem *s_ring = reinterpret_cast<PfItem *>(sb + kOffRing);
     int *s_pref = reinterpret_cast<int *>(sb + kOffPref);
     auto bar = [&](int i) -> uint32_t { return base + kOffBar + i * 8; };
 
@@ -224,14 +228,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                                           PA_DEVERR_TIMEOUT))
                 break;
             int item = 0;
+            if (lane == 0) item = atomicAdd(p.queue, 1);
+            item = __shfl_sync(0xffffffffu, item, 0);
+            PfItem I;
+            if (item < total_items) {
+                I = pf_item(p, s_pref, item);
+                I.end = 0;
+            } else {
+                I.end = 1;
+            }
             if (lane == 0) {
-                item = atomicAdd(p.queue, 1);
-                s_item[slot] = item;
+                s_ring[slot] = I;
                 mbar_arrive(bar(ITEM_FULL + slot));
             }
-            item = __shfl_sync(0xffffffffu, item, 0);
-            if (item >= total_items) break;
-            const PfItem I = pf_item(p, s_pref, item);
+            if (I.end) break;
             if (it > 0 && !mbar_wait(bar(Q_EMPTY), (it - 1) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(Q_FULL), 4 * kHalf);
@@ -303,43 +313,51 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         }
     } else if (warp == kWarpMma) {
         // ================================================== MMA issuer
-        if (lane == 0) {
-            int kt = 0, ia = 0, ib = 0, ta = 0, tb = 0;   // tiles / items seen by tile A and B
-            bool ok = true;
-            auto wait = [&](int b, int ph) -> bool {
-                if (!mbar_wait(bar(b), ph & 1, s_abort, err, PA_DEVERR_TIMEOUT)) {
-                    ok = false;
-                    return false;
-                }
-                return true;
-            };
-            auto qk = [&](uint32_t sQ, int st, uint32_t d_col) {
+        // The whole warp runs the loop and waits (uniform control flow); one
+        // elected lane issues the MMAs and commits.  A tcgen05.mma is accepted
+        // only about one MMA ahead of the tensor core, so each wait between
+        // groups idles the pipe for its latency: every iteration waits at two
+        // points only, each testing all the barriers it needs at once.
+        int kt = 0, ia = 0, ib = 0, ta = 0, tb = 0;   // tiles / items seen by tile A and B
+        bool ok = true;
+        auto waitn = [&](auto const &bars, auto const &pars) -> bool {
+            ok = __all_sync(0xffffffffu, mbar_wait_all(bars, pars, s_abort, err, PA_DEVERR_TIMEOUT));
+            return ok;
+        };
+        auto qk = [&](uint32_t sQ, int st, uint32_t d_col) {
 #pragma unroll
-                for (int kk = 0; kk < kPfD / 16; ++kk) {
-                    const uint64_t a = smem_desc_sw128(sQ + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(sK + st * 2 * kHalf + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-                    umma_ss(tmem + d_col, a, b, kIdescS, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto pv = [&](uint32_t p_col, uint32_t o_col, int st, bool first) {
+            for (int kk = 0; kk < kPfD / 16; ++kk) {
+                const uint64_t a = smem_desc_sw128(sQ + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+                const uint64_t b = smem_desc_sw128(sK + st * 2 * kHalf + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+                umma_ss(tmem + d_col, a, b, kIdescS, kk > 0 ? 1u : 0u);
+            }
+        };
+        auto pv = [&](uint32_t p_col, uint32_t o_col, int st, bool first) {
 #pragma unroll
-                for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-                    const uint64_t b = smem_desc_sw128(sV + st * 2 * kHalf + kk * 2048, kHalf, 1024);
-                    umma_ts(tmem + o_col, tmem + p_col + kk * 8, b, kIdescPV, (kk > 0 || !first) ? 1u : 0u);
-                }
-            };
-            for (int n = 0; ok; ++n) {
-                if (!wait(ITEM_FULL + n % kRing, n / kRing)) break;
-                const int item = s_item[n % kRing];
-                mbar_arrive(bar(ITEM_EMPTY + n % kRing));
-                if (item >= total_items) break;
-                const PfItem I = pf_item(p, s_pref, item);
-                const bool hasB = I.nqb > 0;
-                const int it = ia;   // items so far (every item has a tile A)
-                if (!wait(Q_FULL, it)) break;
-                // S_A(0), S_B(0)
-                if (!wait(K_FULL + (kt & 1), kt >> 1)) break;
-                tc_fence_after();
+            for (int kk = 0; kk < kPfKeys / 16; ++kk) {
+                const uint64_t b = smem_desc_sw128(sV + st * 2 * kHalf + kk * 2048, kHalf, 1024);
+                umma_ts(tmem + o_col, tmem + p_col + kk * 8, b, kIdescPV, (kk > 0 || !first) ? 1u : 0u);
+            }
+        };
+        for (int n = 0; ok; ++n) {
+            const int slot = n % kRing;
+            {
+                const uint32_t b1[1] = {bar(ITEM_FULL + slot)}, p1[1] = {(uint32_t)(n / kRing) & 1u};
+                if (!waitn(b1, p1)) break;
+            }
+            const PfItem I = s_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(ITEM_EMPTY + slot));
+            if (I.end) break;
+            const bool hasB = I.nqb > 0;
+            // S_A(0), S_B(0)
+            {
+                const uint32_t b2[2] = {bar(Q_FULL), bar(K_FULL + (kt & 1))};
+                const uint32_t p2[2] = {(uint32_t)ia & 1u, (uint32_t)(kt >> 1) & 1u};
+                if (!waitn(b2, p2)) break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
                 qk(sQA, kt & 1, 0);
                 umma_commit(bar(SA_FULL));
                 if (hasB) {
@@ -348,48 +366,59 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 }
                 umma_commit(bar(K_EMPTY + (kt & 1)));
                 if (I.ntiles == 1) umma_commit(bar(Q_EMPTY));   // the item's last QK^T: Q may be refilled
-                for (int t = 0; t < I.ntiles; ++t, ++kt) {
-                    const int st = kt & 1, st1 = (kt + 1) & 1;
-                    const bool more = t + 1 < I.ntiles;
-                    // PV_A(t)
-                    if (!wait(PA_FULL, ta) || !wait(V_FULL + st, kt >> 1)) break;
-                    if (t == 0 && ia > 0 && !wait(OA_EMPTY, ia - 1)) break;
-                    tc_fence_after();
-                    pv(0, 256, st, t == 0);
-                    ++ta;
+            }
+            __syncwarp();
+            for (int t = 0; t < I.ntiles; ++t, ++kt) {
+                const int st = kt & 1, st1 = (kt + 1) & 1;
+                const bool more = t + 1 < I.ntiles;
+                // wait point 1: P_A(t), V(t), K(t+1), and O_A free at an item's first tile
+                {
+                    const uint32_t b4[4] = {bar(PA_FULL), bar(V_FULL + st), bar(more ? K_FULL + st1 : V_FULL + st),
+                                            bar(t == 0 && ia > 0 ? OA_EMPTY : V_FULL + st)};
+                    const uint32_t p4[4] = {(uint32_t)ta & 1u, (uint32_t)(kt >> 1) & 1u,
+                                            (uint32_t)(more ? (kt + 1) >> 1 : kt >> 1) & 1u,
+                                            (uint32_t)(t == 0 && ia > 0 ? ia - 1 : kt >> 1) & 1u};
+                    if (!waitn(b4, p4)) break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    pv(0, 256, st, t == 0);                                   // PV_A(t)
                     if (!more) umma_commit(bar(OA_FINAL));
-                    // S_A(t+1)
                     if (more) {
-                        if (!wait(K_FULL + st1, (kt + 1) >> 1)) break;
-                        tc_fence_after();
-                        qk(sQA, st1, 0);
+                        qk(sQA, st1, 0);                                      // S_A(t+1)
                         umma_commit(bar(SA_FULL));
                     }
-                    // PV_B(t)
+                }
+                __syncwarp();
+                ++ta;
+                // wait point 2: P_B(t), and O_B free at an item's first tile
+                if (hasB) {
+                    const uint32_t b2[2] = {bar(PB_FULL), bar(t == 0 && ib > 0 ? OB_EMPTY : PB_FULL)};
+                    const uint32_t p2[2] = {(uint32_t)tb & 1u, (uint32_t)(t == 0 && ib > 0 ? ib - 1 : tb) & 1u};
+                    if (!waitn(b2, p2)) break;
+                    tc_fence_after();
+                }
+                if (elect_one()) {
                     if (hasB) {
-                        if (!wait(PB_FULL, tb)) break;
-                        if (t == 0 && ib > 0 && !wait(OB_EMPTY, ib - 1)) break;
-                        tc_fence_after();
-                        pv(128, 384, st, t == 0);
-                        ++tb;
+                        pv(128, 384, st, t == 0);                             // PV_B(t)
                         if (!more) umma_commit(bar(OB_FINAL));
                     }
                     umma_commit(bar(V_EMPTY + st));
-                    // S_B(t+1)
                     if (more) {
                         if (hasB) {
-                            qk(sQB, st1, 128);
+                            qk(sQB, st1, 128);                                // S_B(t+1)
                             umma_commit(bar(SB_FULL));
                         }
                         umma_commit(bar(K_EMPTY + st1));
                         if (t + 2 == I.ntiles) umma_commit(bar(Q_EMPTY));   // last QK^T of the item issued
                     }
                 }
-                ++ia;
-                if (hasB) ++ib;
+                __syncwarp();
+                if (hasB) ++tb;
             }
+            ++ia;
+            if (hasB) ++ib;
         }
-        __syncwarp();
     } else {
         // ======================= softmax + epilogue: warpgroup X owns tile X
         const int X = warp >> 2;                  // 0: tile A, 1: tile B
@@ -404,11 +433,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         bool ok = true;
         for (int n = 0; ok; ++n) {
             if (!mbar_wait(bar(ITEM_FULL + n % kRing), (n / kRing) & 1, s_abort, err, PA_DEVERR_TIMEOUT)) break;
-            const int item = s_item[n % kRing];
+            const PfItem I = s_ring[n % kRing];
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ITEM_EMPTY + n % kRing));
-            if (item >= total_items) break;
-            const PfItem I = pf_item(p, s_pref, item);
+            if (I.end) break;
             const int nq = X ? I.nqb : I.nqa;
             if (nq <= 0) continue;                // no tile B in this pair
             const int q0 = I.q0 + X * p.TQ;

@@ -67,6 +67,60 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Non-blocking test of a phase: true when the phase with the given parity has completed.
+__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok;
+}
+
+// Wait for the given phases of N barriers together: the first pass tests all
+// of them before looking at any result, so their latencies overlap.  Same
+// time limit and abort protocol as mbar_wait.
+template <int N>
+__device__ __forceinline__ bool mbar_wait_all(const uint32_t (&bar)[N], const uint32_t (&parity)[N],
+                                              volatile int *abort, int32_t *err, int err_bit,
+                                              uint64_t limit_ns = 2000000000ull)
+{
+    uint32_t done[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) done[i] = mbar_test_wait(bar[i], parity[i]);
+    uint32_t all = 1;
+#pragma unroll
+    for (int i = 0; i < N; ++i) all &= done[i];
+    if (all) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        all = 1;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            if (!done[i]) done[i] = mbar_try_wait(bar[i], parity[i]) ? 1u : 0u;
+            all &= done[i];
+        }
+        if (all) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > limit_ns) {
+            *abort = 1;
+            set_error(err, err_bit);
+            return false;
+        }
+    }
+}
+
+// One lane of a converged warp (elect.sync): the lane that issues the warp's
+// tensor-core instructions.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(pred));
+    return pred != 0;
+}
+
 // gpu-scope atomic add with release semantics (prior writes, including those
 // ordered before it by a CTA barrier, are visible before the add)
 __device__ __forceinline__ int atom_add_release_gpu(int *p, int v)
