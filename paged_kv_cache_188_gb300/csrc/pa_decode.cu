@@ -9,9 +9,12 @@
 //
 // How (one kernel, one persistent CTA of 8 warps per SM):
 //  * Planning on the device, redundantly in every CTA: sum of seq_lens ->
-//    split length; per request the split count s_b (<= max_splits); a prefix
-//    sum over s_b * Hkv enumerates work items (b, split, kv head).  The grid
-//    never depends on device lengths, so a captured graph stays valid.
+//    per request the split count s_b (<= max_splits): splits of a common
+//    length (at most 1024 tokens), or -- when batch x Hkv is at most half the
+//    grid and that length would pass 1024 -- counts proportional to the
+//    lengths that fill the grid in one wave; a prefix sum over s_b * Hkv
+//    enumerates work items (b, split, kv head).  The grid never depends on
+//    device lengths, so a captured graph stays valid.
 //  * The CTA's 8 warps share each item: 16-token tile i of the item belongs to
 //    warp i % 8.  Every warp streams its own tiles -- K and V rows of one kv
 //    head, D*2 bytes each wherever the page table puts them -- through a
@@ -34,6 +37,8 @@
 //    writes fp32 (o, m, l) partials and the CTA that completes a (request, kv
 //    head) -- an integer atomic ticket, no waiting -- merges all splits in
 //    split order (deterministic), writes bf16 and re-arms the ticket to zero.
+//    Up to eight splits are merged in one round trip (partials loaded with
+//    the (m, l) pairs); more go weights first, then eight partials at a time.
 //  * No spin-waits: cp.async groups and CTA barriers only.
 #include <math.h>
 
@@ -74,15 +79,31 @@ struct DecodeArgs {
 
 __device__ __forceinline__ int clamp_len(int n, int max_ctx) { return n < 0 ? 0 : (n > max_ctx ? max_ctx : n); }
 
+// How requests are cut into splits.  Large batches: splits of about `chunk`
+// tokens, many items per CTA.  Small batches (budget > 0): one wave -- request
+// b gets floor(budget * n_b / tot) splits, budget = CTAs per kv head, so the
+// items of all requests fill the grid once.
+struct DecPlan {
+    int chunk;
+    int budget;
+    float inv_tot;   // budget / total tokens (every CTA computes the same value)
+};
+
 // split count and split length (tokens) of a request of n tokens
-__device__ __forceinline__ void split_of(int n, int chunk, int max_splits, int &sb, int &len)
+__device__ __forceinline__ void split_of(int n, const DecPlan &pl, int max_splits, int &sb, int &len)
 {
     if (n <= 0) {
         sb = 1;
         len = 0;
         return;
     }
-    int s = (n + chunk - 1) / chunk;
+    int s;
+    if (pl.budget > 0) {
+        s = min((int)((float)n * pl.inv_tot), pl.budget);
+        s = min(max(s, 1), (n + kDecMinChunk - 1) / kDecMinChunk);
+    } else {
+        s = (n + pl.chunk - 1) / pl.chunk;
+    }
     if (s > max_splits) s = max_splits;
     len = ((n + s - 1) / s + 15) & ~15;
     sb = (n + len - 1) / len;
@@ -130,7 +151,7 @@ struct DecItem {
     int row;   // -1 if the request row is invalid
 };
 
-__device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pref, int chunk, int item)
+__device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pref, const DecPlan &chunk, int item)
 {
     int lo = 0, hi = a.batch;   // largest b with s_pref[b] <= item
     while (hi - lo > 1) {
@@ -198,8 +219,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) tot += s_red[w];
     const long long want = (tot * Hkv + gridDim.x - 1) / gridDim.x;
-    int chunk = (int)((want + kDecMinChunk - 1) / kDecMinChunk * kDecMinChunk);
-    chunk = chunk < kDecMinChunk ? kDecMinChunk : (chunk > kDecMaxChunk ? kDecMaxChunk : chunk);
+    DecPlan chunk;
+    chunk.chunk = (int)((want + kDecMinChunk - 1) / kDecMinChunk * kDecMinChunk);
+    chunk.chunk = chunk.chunk < kDecMinChunk ? kDecMinChunk : (chunk.chunk > kDecMaxChunk ? kDecMaxChunk : chunk.chunk);
+    // one wave for small batches whose common split length would hit the cap
+    chunk.budget = (2 * B * Hkv <= (int)gridDim.x && want > kDecMaxChunk) ? (int)gridDim.x / Hkv : 0;
+    chunk.inv_tot = chunk.budget > 0 ? (float)chunk.budget / (float)tot : 0.f;
     {
         const int per = (B + kDecThreads - 1) / kDecThreads;
         const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
@@ -326,7 +351,68 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     // The CTA whose ticket completes (b, h) merges all its splits in split
     // order, writes bf16 and re-arms the ticket.  Whole-CTA; uses the scratch.
     int pend_prev = -1;                        // thread 0: pending ticket result
-    auto merge_splits = [&](int b, int h, int sb) {
+    // few splits (<= 8, typical of large batches): every partial of this
+    // thread's elements is loaded together with the (m, l) pairs -- one
+    // round trip
+    auto merge_few = [&](int b, int h, int sb) {
+        const int hq0 = h * G;
+        float *s_ml = scratch;             // [sb][G][2]
+        float *s_M = s_ml + 2 * sb * G;    // [G]
+        float *s_lt = s_M + G;             // [G]
+        constexpr int EPT = (8 * NH * D + kDecThreads - 1) / kDecThreads;
+        constexpr int PF = 8;
+        const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
+        const float *obase = a.o_part + ((int64_t)b * a.Hq + hq0) * D;
+        float pre[EPT][PF];
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int e = tid + k * kDecThreads;
+#pragma unroll
+            for (int j = 0; j < PF; ++j) pre[k][j] = (e < G * D && j < sb) ? __ldcg(obase + e + j * split_stride) : 0.f;
+        }
+        for (int i = tid; i < sb * G; i += kDecThreads) {
+            const int ss = i / G, gg = i - ss * G;
+            const int64_t pr = ((int64_t)ss * a.cap_batch + b) * a.Hq + hq0 + gg;
+            s_ml[i * 2] = __ldcg(a.ml_part + pr * 2);
+            s_ml[i * 2 + 1] = __ldcg(a.ml_part + pr * 2 + 1);
+        }
+        __syncthreads();
+        for (int gg = tid; gg < G; gg += kDecThreads) {
+            float M = -INFINITY;
+            for (int ss = 0; ss < sb; ++ss) M = fmaxf(M, s_ml[(ss * G + gg) * 2]);
+            const float Mr = M == -INFINITY ? 0.f : M;
+            float lt = 0.f;
+            for (int ss = 0; ss < sb; ++ss) lt += ex2(s_ml[(ss * G + gg) * 2] - Mr) * s_ml[(ss * G + gg) * 2 + 1];
+            s_M[gg] = Mr;
+            s_lt[gg] = lt;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int e = tid + k * kDecThreads;
+            if (e >= G * D) continue;
+            const int gg = e / D;
+            const float Mr = s_M[gg];
+            float acc = 0.f;   // summed in split order
+#pragma unroll
+            for (int j = 0; j < PF; ++j)
+                if (j < sb) acc += ex2(s_ml[(j * G + gg) * 2] - Mr) * pre[k][j];
+            for (int ss = PF; ss < sb; ss += 8) {   // eight loads in flight
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = ss + j < sb ? __ldcg(obase + e + (ss + j) * split_stride) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (ss + j < sb) acc += ex2(s_ml[((ss + j) * G + gg) * 2] - Mr) * v[j];
+            }
+            const float lt = s_lt[gg];
+            a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
+        }
+        if (tid == 0) a.counters[b * Hkv + h] = 0;
+        __syncthreads();
+    };
+    // many splits: weights first, then the partials eight splits at a time
+    auto merge_many = [&](int b, int h, int sb) {
         const int hq0 = h * G;
         float *s_ml = scratch;             // [sb][G][2]
         float *s_w = s_ml + 2 * sb * G;    // [sb][G]
@@ -370,6 +456,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         }
         if (tid == 0) a.counters[b * Hkv + h] = 0;
         __syncthreads();
+    };
+    auto merge_splits = [&](int b, int h, int sb) {
+        if (sb <= 8) merge_few(b, h, sb);
+        else merge_many(b, h, sb);
     };
     // examine the pending ticket (whole CTA): merge if this CTA was last
     auto resolve_ticket = [&]() {
