@@ -73,6 +73,31 @@ typedef struct {
 /* Human-readable name of a status code (static string). */
 const char *pa_status_string(pa_status s);
 
+/* ------------------------------------------------------- launch overlap
+ * Programmatic dependent launch lets a call's kernel start while the kernel
+ * before it on the stream finishes: its CTAs take SMs as the earlier kernel's
+ * CTAs leave, set up shared memory and barriers, and then wait for the earlier
+ * kernel's writes before touching anything it may have written.  Each kernel
+ * lets its successor start only after its own wait, so the overlap never
+ * reaches back further than one kernel.  Process-wide setting, read at each
+ * call (and frozen into a graph at capture):
+ *   PA_OVERLAP_OFF  (default) plain launches.
+ *   PA_OVERLAP_SAFE  overlap; a kernel reads no global memory before its wait.
+ *     Correct in any stream.
+ *   PA_OVERLAP_EARLY_METADATA  overlap, and the index inputs -- seq_lens,
+ *     req_pool_indices, req_to_token, qo_indptr, kv_indptr, positions, loc --
+ *     are read before the wait (the decode and prefill work plans and the
+ *     first page-table entries are ready when the earlier kernel ends).  The
+ *     caller guarantees that the kernel launched immediately before a call on
+ *     its stream does not write those index arrays.  Data (q, k, v, caches,
+ *     tables, workspace, out) are always read after the wait. */
+#define PA_OVERLAP_OFF 0
+#define PA_OVERLAP_SAFE 1
+#define PA_OVERLAP_EARLY_METADATA 2
+/* PA_ERR_SHAPE for an unknown mode. */
+pa_status pa_set_launch_overlap(int mode);
+int pa_get_launch_overlap(void);
+
 /* ----------------------------------------------------------- workspaces
  * A workspace is one caller-allocated device buffer, 256-byte aligned.  Its
  * first 4 bytes are the device error word.  Initialise it once with

@@ -24,6 +24,7 @@ PA_OK = 0
 STATUS = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_SHAPE", 3: "PA_ERR_ALIGN", 4: "PA_ERR_UNSUPPORTED",
           5: "PA_ERR_WORKSPACE", 6: "PA_ERR_CUDA", 7: "PA_ERR_DEVICE_INDEX"}
 DEVERR_SLOT, DEVERR_ROW, DEVERR_LEN, DEVERR_POS = 0x1, 0x2, 0x4, 0x8
+OVERLAP_OFF, OVERLAP_SAFE, OVERLAP_EARLY_METADATA = 0, 1, 2
 
 
 class PaError(RuntimeError):
@@ -39,7 +40,8 @@ class KvShape(ctypes.Structure):
 
 EXPORTS = ["pa_status_string", "pa_decode_workspace_bytes", "pa_prefill_workspace_bytes",
            "pa_workspace_init", "pa_get_error", "pa_get_error_word", "pa_kv_store", "pa_rope_packed",
-           "pa_paged_decode_attn", "pa_paged_prefill_attn", "pa_paged_decode_attn_noalloc"]
+           "pa_paged_decode_attn", "pa_paged_prefill_attn", "pa_paged_decode_attn_noalloc",
+           "pa_set_launch_overlap", "pa_get_launch_overlap"]
 
 _lib = None
 
@@ -71,6 +73,8 @@ def lib():
                                         sz, P, P]
     L.pa_paged_decode_attn_noalloc.argtypes = [P, i32, i32, P, P, KvShape, i32, P, i32, i32, P, P, f32, i32, P,
                                                P, P]
+    L.pa_set_launch_overlap.argtypes = [i32]
+    L.pa_get_launch_overlap.argtypes = []
     for name in EXPORTS[3:]:
         getattr(L, name).restype = i32
     _lib = L
@@ -108,6 +112,15 @@ def _kv_shape(k_buf, v_buf):
     if k_buf.shape != v_buf.shape:
         raise ValueError("k_buf and v_buf shapes differ")
     return KvShape(*k_buf.shape)
+
+
+def pa_set_launch_overlap(mode):
+    """Process-wide launch overlap (OVERLAP_OFF / OVERLAP_SAFE / OVERLAP_EARLY_METADATA)."""
+    _ok("pa_set_launch_overlap", lib().pa_set_launch_overlap(int(mode)))
+
+
+def pa_get_launch_overlap():
+    return int(lib().pa_get_launch_overlap())
 
 
 def pa_decode_workspace_bytes(max_batch, n_q_heads, n_kv_heads, head_dim, max_splits):

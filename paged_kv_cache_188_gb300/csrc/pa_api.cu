@@ -6,6 +6,10 @@
 
 namespace pa {
 
+static volatile int g_overlap = PA_OVERLAP_OFF;
+
+int launch_overlap() { return g_overlap; }
+
 int num_sms()
 {
     static int cached[64] = {0};
@@ -123,3 +127,12 @@ extern "C" pa_status pa_get_error(const void *workspace, int32_t *device_error, 
     if (!aligned256(workspace)) return PA_ERR_ALIGN;
     return pa_get_error_word(static_cast<const int32_t *>(workspace), device_error, st);
 }
+
+extern "C" pa_status pa_set_launch_overlap(int mode)
+{
+    if (mode != PA_OVERLAP_OFF && mode != PA_OVERLAP_SAFE && mode != PA_OVERLAP_EARLY_METADATA) return PA_ERR_SHAPE;
+    pa::g_overlap = mode;
+    return PA_OK;
+}
+
+extern "C" int pa_get_launch_overlap(void) { return pa::g_overlap; }

@@ -63,6 +63,13 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
 }
 
 // barrier over the first `nthreads` threads that use id `id` (warp multiples)
+// Programmatic dependent launch.  pdl_wait: block until the kernel this grid
+// was launched behind has finished and its writes are visible (returns at once
+// for a plain launch).  pdl_launch_dependents: let the next kernel on the
+// stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");

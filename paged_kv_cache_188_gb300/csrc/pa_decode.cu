@@ -39,7 +39,11 @@
 //    split order (deterministic), writes bf16 and re-arms the ticket to zero.
 //    Up to eight splits are merged in one round trip (partials loaded with
 //    the (m, l) pairs); more go weights first, then eight partials at a time.
-//  * No spin-waits: cp.async groups and CTA barriers only.
+//  * Launched behind another kernel (launch overlap on), the CTA waits for it
+//    at the start, or -- early-metadata mode -- after planning and the first
+//    page-table reads, just before its first K/V load.
+//  * Ring waits are bounded in time (PA_DEVERR_TIMEOUT, then the CTA drains
+//    and exits).
 #include <math.h>
 
 #include "pa_internal.h"
@@ -74,6 +78,7 @@ struct DecodeArgs {
     int size, req_rows, max_ctx;
     int cap_batch, max_splits;
     int layer_row0;      // layer_id * size: tensor-map row of slot 0 of the layer
+    int early_meta;      // launched behind another kernel: plan and page table before waiting for it
     float scale_log2;
 };
 
@@ -207,6 +212,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         fence_mbar_init();
     }
     if (tid == 0) *s_abort = 0;
+    if (!a.early_meta) pdl_wait();
 
     // ---------------------------------------------------------- planning
     int my_tot = 0;
@@ -344,6 +350,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         settle(nxt);
     };
 
+    // the plan and the first page-table entries only read index arrays; K/V,
+    // q, the workspace and out wait for the preceding kernel
+    if (a.early_meta) pdl_wait();
+    pdl_launch_dependents();
 #pragma unroll
     for (int i = 0; i < S - 1; ++i) issue();
 
@@ -713,7 +723,7 @@ static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
             return PA_ERR_CUDA;
         configured = smem;
     }
-    kern<<<num_sms(), kDecThreads, smem, st>>>(a);
+    if (launch_kernel(kern, dim3(num_sms()), dim3(kDecThreads), smem, st, a) != cudaSuccess) return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -790,6 +800,7 @@ extern "C" pa_status pa_paged_decode_attn(const void *q, int batch, int n_q_head
     a.cap_batch = ws.cap_batch;
     a.max_splits = max_splits;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.early_meta = launch_overlap() == PA_OVERLAP_EARLY_METADATA;
     if (s.head_dim == 128) return G > 8 ? dispatch_decode<128, 2>(a, st) : dispatch_decode<128, 1>(a, st);
     return G > 8 ? dispatch_decode<64, 2>(a, st) : dispatch_decode<64, 1>(a, st);
 }

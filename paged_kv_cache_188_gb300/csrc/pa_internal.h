@@ -25,6 +25,28 @@ inline bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) &
 // SM count of the current device (cached per device; a property, not call state).
 int num_sms();
 
+// Current launch-overlap mode (PA_OVERLAP_*).
+int launch_overlap();
+
+// Launch `kern` on `st`, as a programmatic dependent of the preceding kernel
+// when launch overlap is on.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = launch_overlap() != PA_OVERLAP_OFF ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 // Encode a TMA tensor map over a bf16 tensor of `rank` (<= 3) dimensions
 // (dims innermost first, strides in bytes for dims 1..rank-1) with the given
 // box, 128-byte swizzle, zero fill out of range.  The driver entry point is

@@ -33,6 +33,9 @@
 //    is rescaled in tensor memory only when the max grows by more than 2^8),
 //    P rounded to bf16 and stored back with tcgen05.st.  Epilogue: O / l to
 //    bf16, rows of padding tokens are not written.
+//  * Launched behind another kernel (launch overlap on), the CTA waits for it
+//    after its barrier and tensor-memory setup, or -- early-metadata mode --
+//    after planning.
 //  * Every mbarrier wait is bounded in time; on a time-out the CTA raises an
 //    abort flag, sets PA_DEVERR_TIMEOUT and unwinds, freeing its TMEM.
 #include <cuda.h>
@@ -86,6 +89,7 @@ struct PrefillParams {
     int32_t *queue;       // [0]: next item to claim, [done]: CTAs finished (kept at 0 between launches)
     int T, Hq, Hkv, G, TQ, R;
     int size, layer_row0, total_rows, req_rows, max_ctx;
+    int early_meta;       // launched behind another kernel: plan before waiting for it
     float scale_log2;
 };
 
@@ -164,10 +168,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         prefetch_tmap(&p.tm_v16);
         prefetch_tmap(&p.tm_v1);
     }
+    if (!p.early_meta) pdl_wait();
 
     // ---------------------------------------------------------- planning
     // q-tile pairs per request (0 for an invalid request), exclusive prefix of
-    // pairs * Hkv; every thread scans a contiguous run of requests
+    // pairs * Hkv; every thread scans a contiguous run of requests.  Error
+    // bits are held until the wait for a preceding kernel.
+    int pend_err = 0;
     {
         const int per = (p.R + kPfThreads - 1) / kPfThreads;
         const int r_lo = min(p.R, tid * per), r_hi = min(p.R, r_lo + per);
@@ -177,15 +184,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
             const int L_r = __ldg(p.kv_indptr + r + 1) - __ldg(p.kv_indptr + r);
             const int row = __ldg(p.req_pool_indices + r);
             if (n_r <= 0) {
-                if (n_r < 0) set_error(err, PA_DEVERR_LEN);
+                if (n_r < 0) pend_err |= PA_DEVERR_LEN;
                 return 0;
             }
             if (qa < 0 || qb > p.T || L_r < n_r || L_r > p.max_ctx) {
-                set_error(err, PA_DEVERR_LEN);
+                pend_err |= PA_DEVERR_LEN;
                 return 0;
             }
             if (row < 0 || row >= p.req_rows) {
-                set_error(err, PA_DEVERR_ROW);
+                pend_err |= PA_DEVERR_ROW;
                 return 0;
             }
             return (n_r + 2 * p.TQ - 1) / (2 * p.TQ);
@@ -210,6 +217,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         if (tid == kPfThreads - 1) s_pref[p.R] = wbase + incl;
     }
     __syncthreads();
+    // the plan read only index arrays; everything below waits for the
+    // preceding kernel
+    if (p.early_meta) pdl_wait();
+    pdl_launch_dependents();
+    if (pend_err) set_error(err, pend_err);
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int total_items = s_pref[p.R];
@@ -642,6 +654,7 @@ extern "C" pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_
     prm.req_rows = req_rows;
     prm.max_ctx = max_ctx;
     prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    prm.early_meta = launch_overlap() == PA_OVERLAP_EARLY_METADATA;
 
     const size_t smem = (size_t)kOffPref + (size_t)(n_reqs + 1) * 4 + 1024;
     static size_t configured = 0;
@@ -651,6 +664,7 @@ extern "C" pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_
             return PA_ERR_CUDA;
         configured = smem;
     }
-    paged_prefill_kernel<<<num_sms(), kPfThreads, smem, st>>>(prm);
+    if (launch_kernel(paged_prefill_kernel, dim3(num_sms()), dim3(kPfThreads), smem, st, prm) != cudaSuccess)
+        return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -7,7 +7,9 @@
 //                    inputs; commit e58a728, docs/developer/architecture.md:
 //                    a real cos/sin freqs_cis table)
 // Both move 16-byte vectors: one thread per 16 bytes of a row, rows contiguous
-// in memory, so every warp touches whole 128-byte lines.
+// in memory, so every warp touches whole 128-byte lines.  Launched behind
+// another kernel (launch overlap on), each thread waits for it before reading
+// data; in early-metadata mode its first loc / position entry is read first.
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -19,13 +21,18 @@ __global__ void __launch_bounds__(256) kv_store_kernel(uint4 *__restrict__ k_lay
                                                        const uint4 *__restrict__ k_new,
                                                        const uint4 *__restrict__ v_new,
                                                        const int32_t *__restrict__ loc, int64_t n_chunks,
-                                                       int row_chunks, int size, int32_t *err)
+                                                       int row_chunks, int size, int32_t *err, int early_meta)
 {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_chunks;
-         i += (int64_t)gridDim.x * blockDim.x) {
+    // early-metadata mode: this thread's first cache location is read before
+    // waiting for the preceding kernel, everything else after
+    const int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    const int32_t slot0 = (early_meta && i0 < n_chunks) ? __ldg(loc + i0 / row_chunks) : 0;
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t i = i0; i < n_chunks; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = i / row_chunks;
         const int c = (int)(i - t * row_chunks);
-        const int32_t slot = __ldg(loc + t);
+        const int32_t slot = (early_meta && i == i0) ? slot0 : __ldg(loc + t);
         if (slot < 0 || slot >= size) {
             if (c == 0) set_error(err, PA_DEVERR_SLOT);
             continue;
@@ -44,16 +51,21 @@ __global__ void __launch_bounds__(256) rope_kernel(uint4 *__restrict__ q, uint4 
                                                    int head_chunks, const int32_t *__restrict__ positions,
                                                    int64_t n_chunks, const float4 *__restrict__ cos_tab,
                                                    const float4 *__restrict__ sin_tab, int max_pos,
-                                                   int32_t *err)
+                                                   int32_t *err, int early_meta)
 {
     const int heads = Hq + Hkv;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_chunks;
-         i += (int64_t)gridDim.x * blockDim.x) {
+    // early-metadata mode: this thread's first position is read before waiting
+    // for the preceding kernel, everything else after
+    const int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    const int32_t p0 = (early_meta && i0 < n_chunks) ? __ldg(positions + i0 / head_chunks / heads) : 0;
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int64_t i = i0; i < n_chunks; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t th = i / head_chunks;     // token * heads + head
         const int c = (int)(i - th * head_chunks);
         const int64_t t = th / heads;
         const int h = (int)(th - t * heads);
-        const int32_t p = __ldg(positions + t);
+        const int32_t p = (early_meta && i == i0) ? p0 : __ldg(positions + t);
         if (p < 0 || p >= max_pos) {
             if (h == 0 && c == 0) set_error(err, PA_DEVERR_POS);
             continue;
@@ -109,10 +121,12 @@ extern "C" pa_status pa_kv_store(void *k_buf, void *v_buf, pa_kv_shape s, int la
     const int row_chunks = s.n_kv_heads * s.head_dim / 8;
     const int64_t layer_off = (int64_t)layer_id * s.size * row_chunks;
     const int64_t n_chunks = (int64_t)n_tokens * row_chunks;
-    kv_store_kernel<<<grid_for(n_chunks, 256), 256, 0, st>>>(
-        static_cast<uint4 *>(k_buf) + layer_off, static_cast<uint4 *>(v_buf) + layer_off,
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), loc, n_chunks, row_chunks, s.size,
-        error_word);
+    if (launch_kernel(kv_store_kernel, dim3(grid_for(n_chunks, 256)), dim3(256), 0, st,
+                      static_cast<uint4 *>(k_buf) + layer_off, static_cast<uint4 *>(v_buf) + layer_off,
+                      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), loc, n_chunks,
+                      row_chunks, s.size, error_word,
+                      (int)(launch_overlap() == PA_OVERLAP_EARLY_METADATA)) != cudaSuccess)
+        return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -130,8 +144,10 @@ extern "C" pa_status pa_rope_packed(void *q, int n_q_heads, void *k, int n_kv_he
     if (error_word && !aligned4(error_word)) return PA_ERR_ALIGN;
     const int head_chunks = head_dim / 8;
     const int64_t n_chunks = (int64_t)n_tokens * (n_q_heads + n_kv_heads) * head_chunks;
-    rope_kernel<<<grid_for(n_chunks, 256), 256, 0, st>>>(
-        static_cast<uint4 *>(q), static_cast<uint4 *>(k), n_q_heads, n_kv_heads, head_chunks, positions, n_chunks,
-        reinterpret_cast<const float4 *>(cos_tab), reinterpret_cast<const float4 *>(sin_tab), max_pos, error_word);
+    if (launch_kernel(rope_kernel, dim3(grid_for(n_chunks, 256)), dim3(256), 0, st, static_cast<uint4 *>(q),
+                      static_cast<uint4 *>(k), n_q_heads, n_kv_heads, head_chunks, positions, n_chunks,
+                      reinterpret_cast<const float4 *>(cos_tab), reinterpret_cast<const float4 *>(sin_tab), max_pos,
+                      error_word, (int)(launch_overlap() == PA_OVERLAP_EARLY_METADATA)) != cudaSuccess)
+        return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

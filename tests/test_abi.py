@@ -105,3 +105,16 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="missing"):
         api.lib()
+
+
+def test_launch_overlap_mode_switch(lib):
+    assert api.pa_get_launch_overlap() == api.OVERLAP_OFF
+    try:
+        for m in (api.OVERLAP_SAFE, api.OVERLAP_EARLY_METADATA, api.OVERLAP_OFF):
+            api.pa_set_launch_overlap(m)
+            assert api.pa_get_launch_overlap() == m
+        assert lib.pa_set_launch_overlap(3) == 2
+        assert lib.pa_set_launch_overlap(-1) == 2
+        assert api.pa_get_launch_overlap() == api.OVERLAP_OFF   # a rejected mode changes nothing
+    finally:
+        api.pa_set_launch_overlap(api.OVERLAP_OFF)
