@@ -37,8 +37,9 @@
 //    writes fp32 (o, m, l) partials and the CTA that completes a (request, kv
 //    head) -- an integer atomic ticket, no waiting -- merges all splits in
 //    split order (deterministic), writes bf16 and re-arms the ticket to zero.
-//    Up to eight splits are merged in one round trip (partials loaded with
-//    the (m, l) pairs); more go weights first, then eight partials at a time.
+//    The ticket is an acquire-release atomic, so the merging CTA needs no
+//    separate fence; the first eight splits' partials travel with the (m, l)
+//    pairs, the weights are warp-parallel, further splits eight at a time.
 //  * Launched behind another kernel (launch overlap on), the CTA waits for it
 //    at the start, or -- early-metadata mode -- after planning and the first
 //    page-table reads, just before its first K/V load.
@@ -360,122 +361,90 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     // ------------------------------------------------------ split merge
     // The CTA whose ticket completes (b, h) merges all its splits in split
     // order, writes bf16 and re-arms the ticket.  Whole-CTA; uses the scratch.
+    // The first eight splits of this thread's output elements are requested
+    // before the (m, l) pairs, so both travel in one round trip; the split
+    // weights are computed warp-parallel (a warp per q head, lanes over
+    // splits, shuffle max and sum).
     int pend_prev = -1;                        // thread 0: pending ticket result
-    // few splits (<= 8, typical of large batches): every partial of this
-    // thread's elements is loaded together with the (m, l) pairs -- one
-    // round trip
-    auto merge_few = [&](int b, int h, int sb) {
+    auto merge_splits = [&](int b, int h, int sb) {
         const int hq0 = h * G;
-        float *s_ml = scratch;             // [sb][G][2]
-        float *s_M = s_ml + 2 * sb * G;    // [G]
-        float *s_lt = s_M + G;             // [G]
+        float *s_w = scratch;              // [sb][G] split weights
+        float *s_lt = s_w + sb * G;        // [G] weighted sums of l
         constexpr int EPT = (8 * NH * D + kDecThreads - 1) / kDecThreads;
-        constexpr int PF = 8;
+        constexpr int SPL = kDecMaxSplits / 32;   // splits per lane
         const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
         const float *obase = a.o_part + ((int64_t)b * a.Hq + hq0) * D;
-        float pre[EPT][PF];
+        float v[EPT][8];
+        auto load8 = [&](int ss) {
 #pragma unroll
-        for (int k = 0; k < EPT; ++k) {
-            const int e = tid + k * kDecThreads;
+            for (int k = 0; k < EPT; ++k) {
+                const int e = tid + k * kDecThreads;
 #pragma unroll
-            for (int j = 0; j < PF; ++j) pre[k][j] = (e < G * D && j < sb) ? __ldcg(obase + e + j * split_stride) : 0.f;
-        }
-        for (int i = tid; i < sb * G; i += kDecThreads) {
-            const int ss = i / G, gg = i - ss * G;
-            const int64_t pr = ((int64_t)ss * a.cap_batch + b) * a.Hq + hq0 + gg;
-            s_ml[i * 2] = __ldcg(a.ml_part + pr * 2);
-            s_ml[i * 2 + 1] = __ldcg(a.ml_part + pr * 2 + 1);
-        }
-        __syncthreads();
-        for (int gg = tid; gg < G; gg += kDecThreads) {
+                for (int j = 0; j < 8; ++j)
+                    v[k][j] = (e < G * D && ss + j < sb) ? __ldcg(obase + e + (ss + j) * split_stride) : 0.f;
+            }
+        };
+        load8(0);
+        const int64_t ml_stride = (int64_t)a.cap_batch * a.Hq * 2;   // floats per split
+        for (int gg = warp; gg < G; gg += kDecWarps) {
+            const float *ml = a.ml_part + ((int64_t)b * a.Hq + hq0 + gg) * 2;
+            float mv[SPL], lv[SPL];
             float M = -INFINITY;
-            for (int ss = 0; ss < sb; ++ss) M = fmaxf(M, s_ml[(ss * G + gg) * 2]);
+#pragma unroll
+            for (int r = 0; r < SPL; ++r) {
+                const int ss = lane + 32 * r;
+                mv[r] = ss < sb ? __ldcg(ml + ss * ml_stride) : -INFINITY;
+                lv[r] = ss < sb ? __ldcg(ml + ss * ml_stride + 1) : 0.f;
+                M = fmaxf(M, mv[r]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
             const float Mr = M == -INFINITY ? 0.f : M;
             float lt = 0.f;
-            for (int ss = 0; ss < sb; ++ss) lt += ex2(s_ml[(ss * G + gg) * 2] - Mr) * s_ml[(ss * G + gg) * 2 + 1];
-            s_M[gg] = Mr;
-            s_lt[gg] = lt;
+#pragma unroll
+            for (int r = 0; r < SPL; ++r) {
+                const int ss = lane + 32 * r;
+                if (ss < sb) {
+                    const float wt = ex2(mv[r] - Mr);
+                    s_w[ss * G + gg] = wt;
+                    lt += wt * lv[r];
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+            if (lane == 0) s_lt[gg] = lt;
         }
         __syncthreads();
+        float acc[EPT];
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) acc[k] = 0.f;
+        for (int ss = 0; ss < sb; ss += 8) {   // each element summed in split order
+            if (ss > 0) load8(ss);
+#pragma unroll
+            for (int k = 0; k < EPT; ++k) {
+                const int e = tid + k * kDecThreads;
+                if (e >= G * D) continue;
+                const int gg = e / D;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (ss + j < sb) acc[k] += s_w[(ss + j) * G + gg] * v[k][j];
+            }
+        }
 #pragma unroll
         for (int k = 0; k < EPT; ++k) {
             const int e = tid + k * kDecThreads;
             if (e >= G * D) continue;
-            const int gg = e / D;
-            const float Mr = s_M[gg];
-            float acc = 0.f;   // summed in split order
-#pragma unroll
-            for (int j = 0; j < PF; ++j)
-                if (j < sb) acc += ex2(s_ml[(j * G + gg) * 2] - Mr) * pre[k][j];
-            for (int ss = PF; ss < sb; ss += 8) {   // eight loads in flight
-                float v[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = ss + j < sb ? __ldcg(obase + e + (ss + j) * split_stride) : 0.f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (ss + j < sb) acc += ex2(s_ml[((ss + j) * G + gg) * 2] - Mr) * v[j];
-            }
-            const float lt = s_lt[gg];
-            a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
+            const float lt = s_lt[e / D];
+            a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc[k] / lt : 0.f);
         }
         if (tid == 0) a.counters[b * Hkv + h] = 0;
         __syncthreads();
-    };
-    // many splits: weights first, then the partials eight splits at a time
-    auto merge_many = [&](int b, int h, int sb) {
-        const int hq0 = h * G;
-        float *s_ml = scratch;             // [sb][G][2]
-        float *s_w = s_ml + 2 * sb * G;    // [sb][G]
-        float *s_lt = s_w + sb * G;        // [G]
-        for (int i = tid; i < sb * G; i += kDecThreads) {
-            const int ss = i / G, gg = i - ss * G;
-            const int64_t pr = ((int64_t)ss * a.cap_batch + b) * a.Hq + hq0 + gg;
-            s_ml[i * 2] = __ldcg(a.ml_part + pr * 2);
-            s_ml[i * 2 + 1] = __ldcg(a.ml_part + pr * 2 + 1);
-        }
-        __syncthreads();
-        for (int gg = tid; gg < G; gg += kDecThreads) {
-            float M = -INFINITY;
-            for (int ss = 0; ss < sb; ++ss) M = fmaxf(M, s_ml[(ss * G + gg) * 2]);
-            const float Mr = M == -INFINITY ? 0.f : M;
-            float lt = 0.f;
-            for (int ss = 0; ss < sb; ++ss) {
-                const float wt = ex2(s_ml[(ss * G + gg) * 2] - Mr);
-                s_w[ss * G + gg] = wt;
-                lt += wt * s_ml[(ss * G + gg) * 2 + 1];
-            }
-            s_lt[gg] = lt;
-        }
-        __syncthreads();
-        const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
-        for (int e = tid; e < G * D; e += kDecThreads) {
-            const int gg = e / D, d = e - gg * D;
-            const float *src = a.o_part + ((int64_t)b * a.Hq + hq0 + gg) * D + d;
-            float acc = 0.f;
-            int ss = 0;
-            for (; ss + 8 <= sb; ss += 8) {   // eight loads in flight, summed in split order
-                float v[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (ss + j) * split_stride);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc += s_w[(ss + j) * G + gg] * v[j];
-            }
-            for (; ss < sb; ++ss) acc += s_w[ss * G + gg] * __ldcg(src + ss * split_stride);
-            const float lt = s_lt[gg];
-            a.out[((int64_t)b * a.Hq + hq0 + gg) * D + d] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
-        }
-        if (tid == 0) a.counters[b * Hkv + h] = 0;
-        __syncthreads();
-    };
-    auto merge_splits = [&](int b, int h, int sb) {
-        if (sb <= 8) merge_few(b, h, sb);
-        else merge_many(b, h, sb);
     };
     // examine the pending ticket (whole CTA): merge if this CTA was last
     auto resolve_ticket = [&]() {
         if (tid == 0) {
+            // the ticket's acquire made the other CTAs' partials visible
             s_flag = pend_prev >= 0 && pend_prev == s_pend[2] - 1;
-            if (s_flag) fence_acq_rel_gpu();   // acquire: the other CTAs' partials are visible
             pend_prev = -1;
         }
         __syncthreads();
@@ -687,12 +656,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         }
         if (I.sb > 1) {
             // ticket for (b, h): the barrier orders every thread's partial
-            // stores before thread 0's release-ordered atomic; its result is
-            // only examined at the next item end (or at exit), so the round
-            // trip overlaps the next item's tiles
+            // stores before thread 0's acquire-release atomic (release: this
+            // CTA's partials; acquire: those of the CTAs that came before, for
+            // the one that completes the count); its result is only examined at
+            // the next item end (or at exit), so the round trip overlaps the
+            // next item's tiles
             __syncthreads();
             if (tid == 0) {
-                pend_prev = atom_add_release_gpu(a.counters + I.b * Hkv + I.h, 1);
+                pend_prev = atom_add_acq_rel_gpu(a.counters + I.b * Hkv + I.h, 1);
                 s_pend[0] = I.b;
                 s_pend[1] = I.h;
                 s_pend[2] = I.sb;

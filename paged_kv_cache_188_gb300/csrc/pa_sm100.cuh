@@ -129,6 +129,13 @@ __device__ __forceinline__ int atom_add_release_gpu(int *p, int v)
     asm volatile("atom.add.release.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+// gpu-scope atomic add with acquire-release semantics
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v)
+{
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // ------------------------------------------------------------------- TMA
