@@ -56,7 +56,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, valid only while the kernel source is unchanged (sha256 prefix).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {"decode": {"sha": "a891aa37c783a684", "ratio": round((537.575424 + 3.885056) / 537.460768, 5),
+                          "capture": "ncu, 4 x 32K tokens, one layer: dram read+write 541.46 MB for "
+                                     "537.46 MB algorithmic; scaled to this workload by algorithmic bytes"}}
 
 
 def parse():
@@ -342,7 +344,9 @@ def run_ours(args, rank, world, local):
     traffic = NCU_TRAFFIC.get("decode")
     traffic_val = None
     if traffic and traffic.get("sha") == src_sha("pa_decode.cu"):
-        traffic_val = traffic.get("bytes_per_launch")
+        # DRAM bytes per launch scale with the K/V bytes streamed: the capture's
+        # traffic / algorithmic ratio times this workload's algorithmic bytes
+        traffic_val = round(traffic["ratio"] * dec_bytes_tot / len(SWEEP))
 
     # end to end: pinned host inputs -> device, step, outputs -> pinned host
     h_in = [t.cpu().pin_memory() for t in (sw.q, sw.k_new, sw.v_new)]
@@ -391,6 +395,7 @@ def run_ours(args, rank, world, local):
         "roofline": {"kernel": "paged_decode_kernel<D=128,S=3,NH=1>", "bound": "hbm", "achieved": round(dec_gbs, 1),
                      "peak": peaks["hbm_gbs"], "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "traffic": traffic_val,
+                     "traffic_source": NCU_TRAFFIC.get("decode", {}).get("capture") if traffic_val else None,
                      "algorithmic_bytes_per_launch": round(dec_bytes_tot / len(SWEEP)),
                      "note": "achieved = algorithmic bytes / CUDA-event time of the decode kernel alone "
                              "(32-layer rotation per context, averaged over the six contexts)"},
@@ -479,6 +484,24 @@ def secondary_workloads(dev, peaks, s):
                      "frac_of_hbm_unique": round(unique / (ms_dec * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
         del st, ws, out, q, kn, g_all, g_dec
         torch.cuda.empty_cache()
+
+    # single-layer B=1 decode (Hq=8, Hkv=2, D=64, 256 tokens): a latency figure
+    # only -- its 128 KiB of K/V stay in L2 -- from a graph of 32 back-to-back calls
+    st = W.config1(device=dev)
+    ws = api.alloc_workspace(api.pa_decode_workspace_bytes(1, 8, 2, 64, MAX_SPLITS), dev)
+    out = torch.empty_like(st.q)
+
+    def calls():
+        for _ in range(32):
+            api.pa_paged_decode_attn(st.q, st.kv.k_buf, st.kv.v_buf, st.layer, st.kv.req_to_token,
+                                     st.kv.req_pool_indices, st.kv.seq_lens, st.scale, ws, MAX_SPLITS, out, stream=s)
+    calls()
+    torch.cuda.synchronize()
+    g1 = capture(calls, s)
+    ms1 = time_graph(g1, 20, s) / 32
+    res["decode_b1_256"] = {"workload": "B=1, Hq=8, Hkv=2, D=64, 256 tokens, page 16", "us_per_call": round(ms1 * 1e3, 3),
+                            "note": "latency only: 128 KiB of K/V, L2-resident"}
+    del st, ws, out, g1
     return res
 
 
