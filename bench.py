@@ -262,6 +262,12 @@ class DecodeSweep:
 
     def layer_call(self, p, l, what=("rope", "store", "decode")):
         a, kv, s = self.api, self.kv, self.stream
+        if tuple(what) == ("rope", "store", "decode"):
+            # the whole step of a layer in one launch
+            a.pa_decode_step(self.q[p, l], self.k_new[p, l], self.v_new[p, l], self.pos[p], self.cos, self.sin,
+                             kv.k_buf, kv.v_buf, l, self.loc[p], kv.req_to_token, kv.req_pool_indices,
+                             self.seq[p], self.scale, self.ws, MAX_SPLITS, self.out[p, l], stream=s)
+            return
         if "rope" in what:
             a.pa_rope_packed(self.q[p, l], self.k_new[p, l], self.pos[p], self.cos, self.sin, self.err, stream=s)
         if "store" in what:
@@ -279,7 +285,7 @@ class DecodeSweep:
         per_layer = [decode_bytes(n) + rope_bytes(1) + store_bytes(1) for n in SWEEP]
         return N_LAYERS * sum(per_layer)
 
-    launches_per_step = 3 * N_LAYERS * len(SWEEP)
+    launches_per_step = N_LAYERS * len(SWEEP)
 
 
 def run_ours(args, rank, world, local):
@@ -379,7 +385,8 @@ def run_ours(args, rank, world, local):
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
-        "config": {"workload": "B=1 paged decode step (RoPE + KV store + split-KV decode), Hq=32 Hkv=8 D=128, "
+        "config": {"workload": "B=1 paged decode step (RoPE + KV store + split-KV decode fused in one launch per "
+                               "layer), Hq=32 Hkv=8 D=128, "
                                "KV [32 layers, 65536 slots, 8, 128] bf16, page 16, contexts 1K-32K x 32 layers",
                    "contexts": SWEEP, "layers": N_LAYERS, "page_size": PAGE, "max_splits": MAX_SPLITS,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -455,6 +462,11 @@ def secondary_workloads(dev, peaks, s):
         q, kn = st.q.clone(), st.k_new.clone()
 
         def stepf(what=("rope", "store", "decode")):
+            if tuple(what) == ("rope", "store", "decode"):
+                api.pa_decode_step(q, kn, st.v_new, st.positions, st.cos_tab, st.sin_tab, st.kv.k_buf, st.kv.v_buf,
+                                   0, st.loc, st.kv.req_to_token, st.kv.req_pool_indices, st.kv.seq_lens, st.scale,
+                                   ws, MAX_SPLITS, out, stream=s)
+                return
             if "rope" in what:
                 api.pa_rope_packed(q, kn, st.positions, st.cos_tab, st.sin_tab, stream=s)
             if "store" in what:

@@ -225,6 +225,34 @@ pa_status pa_paged_decode_attn_noalloc(const void *q, int batch, int n_q_heads, 
                                        float scale, int max_splits, void *out, int32_t *error_word,
                                        cudaStream_t st);
 
+/* ------------------------------------------------------ fused decode step
+ * One layer's decode step in one launch (commit 398e8a3: the CUDA-graph
+ * decode step over packed inputs, rotary embedding on packed 3-D inputs, K/V
+ * stored at buffer[layer_id, loc]).  Same results, bit for bit, as
+ *     pa_rope_packed(q', k', positions, cos_tab, sin_tab)   on copies q', k'
+ *     pa_kv_store(k_buf, v_buf, layer_id, k', v_new, loc)
+ *     pa_paged_decode_attn(q', ...)
+ * with one new token per request:
+ *   q: bf16 [batch, n_q_heads, head_dim]; k_new, v_new: bf16 [batch,
+ *   n_kv_heads, head_dim]; q and k_new are only read (the rotated q stays in
+ *   registers, the rotated k goes to the cache).
+ *   positions: int32 [batch], the new token's rotary position; cos_tab,
+ *   sin_tab: fp32 [max_pos, head_dim / 2].
+ *   loc: int32 [batch], the new token's slot.  It must be the request's last
+ *   position, loc[b] == req_to_token[req_pool_indices[b], seq_lens[b] - 1]:
+ *   the row is written by the one CTA that reads it, just before it reads it.
+ *   A mismatch sets PA_DEVERR_SLOT (the row is still written at loc[b]).
+ *   k_buf, v_buf: written at [layer_id, loc[b]], then read for attention.
+ * Everything else, the workspace and the limits are those of
+ * pa_paged_decode_attn.  A position outside [0, max_pos) sets PA_DEVERR_POS
+ * and leaves that token's q and k unrotated, as pa_rope_packed does. */
+pa_status pa_decode_step(const void *q, const void *k_new, const void *v_new, int batch, int n_q_heads,
+                         const int32_t *positions, const float *cos_tab, const float *sin_tab, int max_pos,
+                         void *k_buf, void *v_buf, pa_kv_shape s, int layer_id, const int32_t *loc,
+                         const int32_t *req_to_token, int req_rows, int max_ctx,
+                         const int32_t *req_pool_indices, const int32_t *seq_lens, float scale,
+                         void *workspace, size_t workspace_bytes, int max_splits, void *out, cudaStream_t st);
+
 /* ----------------------------------------------------------- prefill attn
  * Commit e58a728: packed prompts with a shared prefix start in one forward,
  * paged prefill (attn_paged_prefill), rows located by cumulative query lengths;

@@ -41,7 +41,7 @@ class KvShape(ctypes.Structure):
 EXPORTS = ["pa_status_string", "pa_decode_workspace_bytes", "pa_prefill_workspace_bytes",
            "pa_workspace_init", "pa_get_error", "pa_get_error_word", "pa_kv_store", "pa_rope_packed",
            "pa_paged_decode_attn", "pa_paged_prefill_attn", "pa_paged_decode_attn_noalloc",
-           "pa_set_launch_overlap", "pa_get_launch_overlap"]
+           "pa_set_launch_overlap", "pa_get_launch_overlap", "pa_decode_step"]
 
 _lib = None
 
@@ -73,6 +73,8 @@ def lib():
                                         sz, P, P]
     L.pa_paged_decode_attn_noalloc.argtypes = [P, i32, i32, P, P, KvShape, i32, P, i32, i32, P, P, f32, i32, P,
                                                P, P]
+    L.pa_decode_step.argtypes = [P, P, P, i32, i32, P, P, P, i32, P, P, KvShape, i32, P, P, i32, i32, P, P, f32,
+                                 P, sz, i32, P, P]
     L.pa_set_launch_overlap.argtypes = [i32]
     L.pa_get_launch_overlap.argtypes = []
     for name in EXPORTS[3:]:
@@ -209,6 +211,35 @@ def pa_paged_decode_attn(q, k_buf, v_buf, layer_id, req_to_token, req_pool_indic
         _p(q), B, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(req_to_token), req_to_token.shape[0],
         req_to_token.shape[1], _p(req_pool_indices), _p(seq_lens), float(scale), _p(workspace),
         workspace.numel(), max_splits, _p(out), _stream(stream)))
+
+
+def pa_decode_step(q, k_new, v_new, positions, cos_tab, sin_tab, k_buf, v_buf, layer_id, loc, req_to_token,
+                   req_pool_indices, seq_lens, scale, workspace, max_splits, out, stream=None):
+    """RoPE + KV store + decode attention of one layer in one launch (q, k_new only read)."""
+    s = _kv_shape(k_buf, v_buf)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(positions, torch.int32, "positions", 1)
+    _need(loc, torch.int32, "loc", 1)
+    _need(cos_tab, torch.float32, "cos_tab", 2)
+    _need(sin_tab, torch.float32, "sin_tab", 2)
+    _need(req_to_token, torch.int32, "req_to_token", 2)
+    _need(req_pool_indices, torch.int32, "req_pool_indices", 1)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(workspace, torch.uint8, "workspace")
+    B, Hq, D = q.shape
+    if (out.shape != q.shape or D != s.head_dim or k_new.shape != (B, s.n_kv_heads, D) or v_new.shape != k_new.shape
+            or positions.numel() != B or loc.numel() != B or req_pool_indices.numel() != B or seq_lens.numel() != B
+            or cos_tab.shape != sin_tab.shape or cos_tab.shape[1] != D // 2):
+        raise ValueError("q/out [batch, Hq, D], k_new/v_new [batch, Hkv, D], positions/loc/req_pool_indices/"
+                         "seq_lens [batch], cos/sin [max_pos, D/2] expected")
+    _ok("pa_decode_step", lib().pa_decode_step(
+        _p(q), _p(k_new), _p(v_new), B, Hq, _p(positions), _p(cos_tab), _p(sin_tab), cos_tab.shape[0],
+        _p(k_buf), _p(v_buf), s, layer_id, _p(loc), _p(req_to_token), req_to_token.shape[0], req_to_token.shape[1],
+        _p(req_pool_indices), _p(seq_lens), float(scale), _p(workspace), workspace.numel(), max_splits, _p(out),
+        _stream(stream)))
 
 
 def pa_paged_decode_attn_noalloc(q, k_buf, v_buf, layer_id, req_to_token, req_pool_indices, seq_lens, scale,

@@ -97,6 +97,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Rotate one interleaved bf16 pair (x0, x1) stored as a 32-bit word by the
+// angle with cosine c and sine s: (x0*c - x1*s, x0*s + x1*c), rounded to bf16
+// (nearest even).  The products x1*s and x1*c are split exactly into p + e
+// (FMA remainder), so a cancelling sum keeps its low bits.  Shared by the RoPE
+// kernel and the fused decode step so both give the same bits.
+__device__ __forceinline__ uint32_t rope_pair_bf16(uint32_t w, float c, float s)
+{
+    const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+    const float x0 = __low2float(pr), x1 = __high2float(pr);
+    const float p0 = x1 * s, e0 = fmaf(x1, s, -p0);
+    const float p1 = x1 * c, e1 = fmaf(x1, c, -p1);
+    const float y0 = fmaf(x0, c, -p0) - e0;
+    const float y1 = fmaf(x0, s, p1) + e1;
+    return pack_bf16x2(y0, y1);
+}
+
 __device__ __forceinline__ float fast_exp2(float x)
 {
     return exp2f(x);

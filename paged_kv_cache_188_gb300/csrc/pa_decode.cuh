@@ -1,0 +1,920 @@
+#pragma once
+// pa_decode.cuh -- packed GQA split-KV decode attention over the paged cache:
+// the kernel and its launch, shared by pa_decode.cu (decode attention, and
+// the allocation-free entry point) and pa_decode_step.cu (the fused step).
+//
+// What it computes (AstrAI commit 398e8a3, tests/inference/test_cache.py:
+// packed decode with int32 req_to_token / req_pool_indices / seq_lens and
+// workspace-owned split partials decode_o_part / decode_ml_part; commit
+// e58a728, docs/developer/architecture.md: decode reads K/V via req_to_token):
+// for request b and query head hq, softmax(scale * q K^T) V over the request's
+// seq_lens[b] cached tokens, K/V rows gathered through req_to_token.
+//
+// How (one kernel, one persistent CTA of 8 warps per SM):
+//  * Planning on the device, redundantly in every CTA: sum of seq_lens ->
+//    per request the split count s_b (<= max_splits): splits of a common
+//    length (at most 1024 tokens), or -- when batch x Hkv is at most half the
+//    grid and that length would pass 1024 -- counts proportional to the
+//    lengths that fill the grid in one wave; a prefix sum over s_b * Hkv
+//    enumerates work items (b, split, kv head).  The grid never depends on
+//    device lengths, so a captured graph stays valid.
+//  * The CTA's 8 warps share each item: 16-token tile i of the item belongs to
+//    warp i % 8.  Every warp streams its own tiles -- K and V rows of one kv
+//    head, D*2 bytes each wherever the page table puts them -- through a
+//    private ring of S shared-memory stages with 16-byte cp.async copies (D/8
+//    lanes per row, so an instruction reads whole rows).  The ring runs across
+//    item boundaries: while a warp computes its last tiles of one item it is
+//    already loading its first tiles of the next.  Page-table entries of the
+//    next tile to load are prefetched into registers one tile ahead.  Rows are
+//    stored with a 16-byte-chunk XOR swizzle so ldmatrix is conflict free.
+//    (A gather microbenchmark on this GPU: 8 warps x 3 cp.async stages per SM
+//    read these rows at 7.2 TB/s; a single TMA-issuing thread per SM tops out
+//    near 4.4 TB/s.)
+//  * Per tile, warp-level bf16 MMAs (m16n8k16) with tokens as the M dimension:
+//      S^T[tok, head] = K[tok, :] . Q[head, :]       (Q^T held in registers)
+//      online softmax per head column, log2 domain (exp2)
+//      O^T[d, head]  += V^T[d, tok] . P^T[tok, head]   (P^T by movmatrix)
+//    so K/V bytes are read once for all G heads of the kv head.
+//  * At the end of an item the warps' states merge in shared memory; a
+//    request with one split writes bf16 output directly, otherwise the item
+//    writes fp32 (o, m, l) partials and the CTA that completes a (request, kv
+//    head) -- an integer atomic ticket, no waiting -- merges all splits in
+//    split order (deterministic), writes bf16 and re-arms the ticket to zero.
+//    The ticket is an acquire-release atomic, so the merging CTA needs no
+//    separate fence; the first eight splits' partials travel with the (m, l)
+//    pairs, the weights are warp-parallel, further splits eight at a time.
+//  * Fused decode step (FUSED = true, pa_decode_step): q is rotated (RoPE)
+//    in registers as it is loaded, and the CTA holding the last split of a
+//    (request, kv head) writes that head's new K (rotated) and V rows at
+//    loc[b] before it loads any tile; it is the only CTA that reads them.
+//  * Launched behind another kernel (launch overlap on), the CTA waits for it
+//    at the start, or -- early-metadata mode -- after planning and the first
+//    page-table reads, just before its first K/V load.
+//  * Ring waits are bounded in time (PA_DEVERR_TIMEOUT, then the CTA drains
+//    and exits).
+#include <math.h>
+
+#include "pa_internal.h"
+#include "pa_sm100.cuh"
+
+namespace pa {
+using namespace sm100;
+
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kDecTile = 16;        // tokens per ring stage
+constexpr int kDecMinChunk = 64;    // split length bounds (tokens)
+constexpr int kDecMaxChunk = 1024;
+constexpr int kDecMaxBatch = 4096;
+constexpr int kDecMaxSplits = 128;
+
+struct DecodeArgs {
+    CUtensorMap tm_k;    // 2-D (element, row) over k_buf rows, 64 x 16 boxes, 128-byte swizzle
+    CUtensorMap tm_v;
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_layer;
+    const __nv_bfloat16 *v_layer;
+    const int32_t *req_to_token;
+    const int32_t *req_pool_indices;
+    const int32_t *seq_lens;
+    __nv_bfloat16 *out;
+    int32_t *err;
+    int32_t *counters;
+    float *ml_part;
+    float *o_part;
+    int batch, Hq, Hkv, G;
+    int size, req_rows, max_ctx;
+    int cap_batch, max_splits;
+    int layer_row0;      // layer_id * size: tensor-map row of slot 0 of the layer
+    int early_meta;      // launched behind another kernel: plan and page table before waiting for it
+    float scale_log2;
+    // fused decode step (k_new != null): RoPE on q as it is loaded, and the new
+    // token's rotated K and its V written at loc[b] before any tile is read
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    const int32_t *positions;
+    const int32_t *loc;
+    const float *cos_tab;
+    const float *sin_tab;
+    __nv_bfloat16 *k_layer_w;   // the layer's K / V rows, writable
+    __nv_bfloat16 *v_layer_w;
+    int max_pos;
+};
+
+__device__ __forceinline__ int clamp_len(int n, int max_ctx) { return n < 0 ? 0 : (n > max_ctx ? max_ctx : n); }
+
+// How requests are cut into splits.  Large batches: splits of about `chunk`
+// tokens, many items per CTA.  Small batches (budget > 0): one wave -- request
+// b gets floor(budget * n_b / tot) splits, budget = CTAs per kv head, so the
+// items of all requests fill the grid once.
+struct DecPlan {
+    int chunk;
+    int budget;
+    float inv_tot;   // budget / total tokens (every CTA computes the same value)
+};
+
+// split count and split length (tokens) of a request of n tokens
+__device__ __forceinline__ void split_of(int n, const DecPlan &pl, int max_splits, int &sb, int &len)
+{
+    if (n <= 0) {
+        sb = 1;
+        len = 0;
+        return;
+    }
+    int s;
+    if (pl.budget > 0) {
+        s = min((int)((float)n * pl.inv_tot), pl.budget);
+        s = min(max(s, 1), (n + kDecMinChunk - 1) / kDecMinChunk);
+    } else {
+        s = (n + pl.chunk - 1) / pl.chunk;
+    }
+    if (s > max_splits) s = max_splits;
+    len = ((n + s - 1) / s + 15) & ~15;
+    sb = (n + len - 1) / len;
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Shared memory (from a 1024-byte aligned base): per-warp rings
+// [warp][S][K tile | V tile], each tile D/64 halves of 16 rows x 128 B with the
+// 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)) -- the
+// layout TMA writes and the cp.async path reproduces; consumer scratch;
+// per-warp stage validity masks and mbarriers; the plan's prefix array.
+template <int D, int S, int NH>
+struct DecSmem {
+    static constexpr int kHalf = kDecTile * 128;                         // 16 rows x 128 B
+    static constexpr int kTile = (D / 64) * kHalf;                       // one K or V tile
+    static constexpr int kStage = 2 * kTile;
+    static constexpr int kRing = S * kStage;                             // per warp
+    static constexpr int kScratchOff = kDecWarps * kRing;
+    // half the warps' O states [4][G][D] fp32 at a time, later the split merge
+    // [sb][G][2] + [sb][G] + [G]
+    static constexpr int kCombine = (kDecWarps / 2) * 8 * NH * D * 4;
+    static constexpr int kMerge = (3 * kDecMaxSplits * 8 * NH + 8 * NH) * 4;
+    static constexpr int kScratch = kCombine > kMerge ? kCombine : kMerge;
+    static constexpr int kMaskOff = kScratchOff + kScratch;
+    static constexpr int kBarOff = kMaskOff + kDecWarps * S * 4;
+    static constexpr int kPrefOff = kBarOff + kDecWarps * S * 8;
+    static constexpr size_t bytes(int batch) { return 1024 + (size_t)kPrefOff + (size_t)(batch + 1) * 4; }
+    // byte offset of 16-byte chunk c of row r inside a K or V tile
+    __device__ static __forceinline__ uint32_t off(int r, int c)
+    {
+        return (uint32_t)((c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    }
+};
+constexpr size_t kSmemLimit = 232448 - 4096;   // opt-in maximum minus static shared memory (with margin)
+
+// Everything an item needs, derived from the plan (identical in every warp).
+struct DecItem {
+    int b, s, h, sb, t0, t1, ntiles;
+    int row;   // -1 if the request row is invalid
+};
+
+// request of a work item: the largest b with s_pref[b] <= item (shared memory only)
+__device__ __forceinline__ int item_request(const int *s_pref, int batch, int item)
+{
+    int lo = 0, hi = batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pref[mid] <= item) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pref, const DecPlan &chunk, int item)
+{
+    const int lo = item_request(s_pref, a.batch, item);
+    DecItem I;
+    I.b = lo;
+    const int local = item - s_pref[lo];
+    I.s = local / a.Hkv;
+    I.h = local - I.s * a.Hkv;
+    int n = clamp_len(__ldg(a.seq_lens + lo), a.max_ctx);
+    int len;
+    split_of(n, chunk, a.max_splits, I.sb, len);
+    I.row = __ldg(a.req_pool_indices + lo);
+    if (I.row < 0 || I.row >= a.req_rows) {
+        I.row = -1;
+        n = 0;
+    }
+    I.t0 = I.s * len;
+    I.t1 = min(n, I.t0 + len);
+    I.ntiles = I.t1 > I.t0 ? (I.t1 - I.t0 + kDecTile - 1) / kDecTile : 0;
+    return I;
+}
+
+template <int D, int S, int NH, bool FUSED>
+__global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __grid_constant__ DecodeArgs a)
+{
+    using L = DecSmem<D, S, NH>;
+    constexpr int KSTEPS = D / 16;
+    constexpr int DM = D / 16;         // 16-row d tiles of O^T
+    constexpr int CPR = D / 8;         // 16-byte chunks per row
+    constexpr int TPI = 32 / CPR;      // rows per warp-wide copy instruction
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + (((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw));
+    float *scratch = reinterpret_cast<float *>(smem + L::kScratchOff);
+    uint32_t *s_vmask = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
+    int32_t *s_pref = reinterpret_cast<int32_t *>(smem + L::kPrefOff);
+    __shared__ float s_m[kDecWarps][16], s_l[kDecWarps][16];
+    __shared__ int s_red[kDecWarps];
+    __shared__ int s_flag, s_pend[3];
+    __shared__ int s_abort_storage;
+    __shared__ int s_step_n;
+    __shared__ int32_t s_pos[FUSED ? kDecThreads : 1];   // fused step: positions[b] of this CTA's first items
+    volatile int *s_abort = &s_abort_storage;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int B = a.batch, Hkv = a.Hkv, G = a.G;
+    const uint32_t bars = smem_u32(smem + L::kBarOff) + warp * S * 8;   // this warp's stage barriers
+    if (lane == 0) {
+        // 32 lanes' cp.async completions + lane 0's arrival carrying the TMA bytes
+        for (int i = 0; i < S; ++i) mbar_init(bars + i * 8, 33);
+        fence_mbar_init();
+    }
+    if (tid == 0) *s_abort = 0;
+    if (!a.early_meta) pdl_wait();
+
+    // ---------------------------------------------------------- planning
+    int my_tot = 0;
+    for (int b = tid; b < B; b += kDecThreads) my_tot += clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) my_tot += __shfl_xor_sync(0xffffffffu, my_tot, o);
+    if (lane == 0) s_red[warp] = my_tot;
+    __syncthreads();
+    long long tot = 0;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) tot += s_red[w];
+    const long long want = (tot * Hkv + gridDim.x - 1) / gridDim.x;
+    DecPlan chunk;
+    chunk.chunk = (int)((want + kDecMinChunk - 1) / kDecMinChunk * kDecMinChunk);
+    chunk.chunk = chunk.chunk < kDecMinChunk ? kDecMinChunk : (chunk.chunk > kDecMaxChunk ? kDecMaxChunk : chunk.chunk);
+    // one wave for small batches whose common split length would hit the cap
+    chunk.budget = (2 * B * Hkv <= (int)gridDim.x && want > kDecMaxChunk) ? (int)gridDim.x / Hkv : 0;
+    chunk.inv_tot = chunk.budget > 0 ? (float)chunk.budget / (float)tot : 0.f;
+    {
+        const int per = (B + kDecThreads - 1) / kDecThreads;
+        const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
+        int run = 0;
+        for (int b = b_lo; b < b_hi; ++b) {
+            int sb, len;
+            split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), chunk, a.max_splits, sb, len);
+            run += sb * Hkv;
+        }
+        int incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        __syncthreads();   // s_red reuse
+        if (lane == 31) s_red[warp] = incl;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += s_red[w];
+        int excl = base + incl - run;
+        for (int b = b_lo; b < b_hi; ++b) {
+            s_pref[b] = excl;
+            int sb, len;
+            split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), chunk, a.max_splits, sb, len);
+            excl += sb * Hkv;
+        }
+        if (tid == kDecThreads - 1) s_pref[B] = base + incl;
+    }
+    __syncthreads();
+    const int total_items = s_pref[B];
+    const int64_t slot_stride = (int64_t)Hkv * D;
+    const uint32_t ring = smem_u32(smem) + warp * L::kRing;
+    bool bad = false;   // a ring wait timed out: skip work, keep the barriers
+
+    // ------------------------------------------- this warp's load cursors
+    // a cursor walks (item, tile) pairs in the order the warp computes them:
+    // tiles warp, warp+8, ... of the CTA's items blockIdx.x, +gridDim.x, ...
+    // `cur` is the next tile to load, `nxt` the one after; both hold their
+    // page-table entries (lane t < 16: token t), fetched when the cursor moved
+    struct Cursor {
+        int item, tile, slot;
+        DecItem I;
+    };
+    auto settle = [&](Cursor &c) {
+        while (c.item < total_items && c.tile >= c.I.ntiles) {
+            c.item += gridDim.x;
+            c.tile = warp;
+            if (c.item < total_items) c.I = dec_item(a, s_pref, chunk, c.item);
+        }
+        c.slot = -1;
+        if (c.item < total_items && lane < kDecTile && c.I.row >= 0) {
+            const int tok = c.I.t0 + c.tile * kDecTile + lane;
+            if (tok < c.I.t1) c.slot = __ldg(a.req_to_token + (int64_t)c.I.row * a.max_ctx + tok);
+        }
+    };
+    Cursor cur;
+    cur.item = blockIdx.x;
+    cur.tile = warp;
+    cur.I.ntiles = 0;
+    cur.I.row = -1;
+    cur.I.t0 = cur.I.t1 = cur.I.h = 0;
+    if (cur.item < total_items) cur.I = dec_item(a, s_pref, chunk, cur.item);
+    settle(cur);
+    Cursor nxt = cur;
+    nxt.tile += kDecWarps;
+    settle(nxt);
+    int n_issued = 0;
+    // load the `cur` tile into ring stage n_issued % S, then advance both cursors
+    auto issue = [&]() {
+        if (cur.item >= total_items) return;
+        const int st = n_issued % S;
+        const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile, fb = bars + st * 8;
+        const int tok0 = cur.I.t0 + cur.tile * kDecTile;
+        int sl = cur.slot;
+        const bool in_range = lane < kDecTile && tok0 + lane < cur.I.t1;
+        if (in_range && (sl < 0 || sl >= a.size)) set_error(a.err, PA_DEVERR_SLOT);
+        const bool ok = in_range && sl >= 0 && sl < a.size;
+        if (!ok) sl = -1;
+        const unsigned vmask = __ballot_sync(0xffffffffu, ok);
+        // 16 tokens on 16 consecutive slots (one page): four TMA boxes
+        const int s0 = __shfl_sync(0xffffffffu, sl, 0);
+        const bool page = (__ballot_sync(0xffffffffu, ok && sl == s0 + lane) & 0xFFFFu) == 0xFFFFu;
+        if (lane == 0) {
+            s_vmask[warp * S + st] = vmask;
+            mbar_arrive_expect_tx(fb, page ? 2u * L::kTile : 0u);
+        }
+        __syncwarp();
+        const int h = cur.I.h;
+        if (page) {
+            if (lane == 0) {
+#pragma unroll
+                for (int hh = 0; hh < D / 64; ++hh) {
+                    tma_load_2d(kb + hh * L::kHalf, &a.tm_k, h * D + hh * 64, a.layer_row0 + s0, fb);
+                    tma_load_2d(vb + hh * L::kHalf, &a.tm_v, h * D + hh * 64, a.layer_row0 + s0, fb);
+                }
+            }
+        } else {
+            const __nv_bfloat16 *kh = a.k_layer + (int64_t)h * D;
+            const __nv_bfloat16 *vh = a.v_layer + (int64_t)h * D;
+#pragma unroll
+            for (int j = 0; j < kDecTile / TPI; ++j) {
+                const int r = j * TPI + lane / CPR;
+                const int ch = lane % CPR;
+                const int rs = __shfl_sync(0xffffffffu, sl, r);
+                const int64_t off = rs >= 0 ? (int64_t)rs * slot_stride + ch * 8 : 0;
+                const int nb = rs >= 0 ? 16 : 0;      // masked rows: zero fill, no read
+                const uint32_t o = L::off(r, ch);
+                cp_async_16(kb + o, kh + off, nb);
+                cp_async_16(vb + o, vh + off, nb);
+            }
+        }
+        cp_async_arrive_noinc(fb);
+        ++n_issued;
+        cur = nxt;
+        nxt.tile += kDecWarps;
+        settle(nxt);
+    };
+
+    // the plan and the first page-table entries only read index arrays; K/V,
+    // q, the workspace and out wait for the preceding kernel
+    // Fused step, part 1 (index reads only, so ahead of the wait in
+    // early-metadata mode): every thread examines one of this CTA's items;
+    // the last split of each (request, kv head) -- the only item that reads
+    // the new token -- goes on a list in the scratch (request, kv head, slot,
+    // position).  Part 2, after the wait: groups of 2*D/8 lanes write those
+    // rows (K rotated, V as is), an async-proxy fence and the CTA barrier
+    // order them before this CTA's own TMA / cp.async reads.
+    constexpr int STEP_GROUP = 2 * (D / 8);                 // lanes per row pair (16-byte chunks of K and V)
+    int4 *s_list = reinterpret_cast<int4 *>(scratch);
+    static_assert(L::kScratch >= kDecThreads * (int)sizeof(int4), "step list fits the scratch");
+    int step_err = 0;
+    auto collect = [&](int pass) -> bool {   // whole CTA; false once the CTA has no more items
+        if (tid == 0) s_step_n = 0;
+        __syncthreads();
+        const int first = blockIdx.x + pass * kDecThreads * (int)gridDim.x;
+        const int item = first + tid * (int)gridDim.x;
+        if (item < total_items) {
+            const DecItem I = dec_item(a, s_pref, chunk, item);
+            const int32_t p = __ldg(a.positions + I.b);
+            if (pass == 0) s_pos[tid] = p;   // the q rotation of item tid needs no global load later
+            if (I.s == I.sb - 1) {
+                const int32_t slot = __ldg(a.loc + I.b);
+                if (p < 0 || p >= a.max_pos) step_err |= PA_DEVERR_POS;
+                if (slot < 0 || slot >= a.size ||
+                    (I.row >= 0 && I.t1 > 0 && __ldg(a.req_to_token + (int64_t)I.row * a.max_ctx + I.t1 - 1) != slot))
+                    step_err |= PA_DEVERR_SLOT;
+                if (slot >= 0 && slot < a.size) s_list[atomicAdd(&s_step_n, 1)] = make_int4(I.b, I.h, slot, p);
+            }
+        }
+        __syncthreads();
+        return first < total_items;
+    };
+    auto store_rows = [&]() {   // whole CTA
+        const int n = s_step_n;
+        const int li = tid % STEP_GROUP;
+        const bool isv = li >= STEP_GROUP / 2;
+        const int c = li - (isv ? STEP_GROUP / 2 : 0);
+        for (int e = tid / STEP_GROUP; e < n; e += kDecThreads / STEP_GROUP) {
+            const int4 E = s_list[e];
+            const int64_t src = ((int64_t)E.x * Hkv + E.y) * D;
+            uint4 x = __ldg(reinterpret_cast<const uint4 *>((isv ? a.v_new : a.k_new) + src) + c);
+            if (!isv && E.w >= 0 && E.w < a.max_pos) {
+                const float4 cs = __ldg(reinterpret_cast<const float4 *>(a.cos_tab + (int64_t)E.w * (D / 2)) + c);
+                const float4 sn = __ldg(reinterpret_cast<const float4 *>(a.sin_tab + (int64_t)E.w * (D / 2)) + c);
+                x = make_uint4(rope_pair_bf16(x.x, cs.x, sn.x), rope_pair_bf16(x.y, cs.y, sn.y),
+                               rope_pair_bf16(x.z, cs.z, sn.z), rope_pair_bf16(x.w, cs.w, sn.w));
+            }
+            __nv_bfloat16 *dst = (isv ? a.v_layer_w : a.k_layer_w) + (int64_t)E.z * slot_stride + (int64_t)E.y * D;
+            reinterpret_cast<uint4 *>(dst)[c] = x;
+        }
+    };
+    bool more_steps = false;
+    if (FUSED) more_steps = collect(0);
+    if (a.early_meta) pdl_wait();
+    pdl_launch_dependents();
+    if (FUSED) {
+        for (int pass = 1; more_steps; ++pass) {
+            store_rows();
+            __syncthreads();   // list reuse
+            more_steps = collect(pass);
+        }
+        if (step_err) set_error(a.err, step_err);
+        fence_proxy_async_global();
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < S - 1; ++i) issue();
+
+    // ------------------------------------------------------ split merge
+    // The CTA whose ticket completes (b, h) merges all its splits in split
+    // order, writes bf16 and re-arms the ticket.  Whole-CTA; uses the scratch.
+    // The first eight splits of this thread's output elements are requested
+    // before the (m, l) pairs, so both travel in one round trip; the split
+    // weights are computed warp-parallel (a warp per q head, lanes over
+    // splits, shuffle max and sum).
+    int pend_prev = -1;                        // thread 0: pending ticket result
+    auto merge_splits = [&](int b, int h, int sb) {
+        const int hq0 = h * G;
+        float *s_w = scratch;              // [sb][G] split weights
+        float *s_lt = s_w + sb * G;        // [G] weighted sums of l
+        constexpr int EPT = (8 * NH * D + kDecThreads - 1) / kDecThreads;
+        constexpr int SPL = kDecMaxSplits / 32;   // splits per lane
+        const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
+        const float *obase = a.o_part + ((int64_t)b * a.Hq + hq0) * D;
+        float v[EPT][8];
+        auto load8 = [&](int ss) {
+#pragma unroll
+            for (int k = 0; k < EPT; ++k) {
+                const int e = tid + k * kDecThreads;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    v[k][j] = (e < G * D && ss + j < sb) ? __ldcg(obase + e + (ss + j) * split_stride) : 0.f;
+            }
+        };
+        load8(0);
+        const int64_t ml_stride = (int64_t)a.cap_batch * a.Hq * 2;   // floats per split
+        for (int gg = warp; gg < G; gg += kDecWarps) {
+            const float *ml = a.ml_part + ((int64_t)b * a.Hq + hq0 + gg) * 2;
+            float mv[SPL], lv[SPL];
+            float M = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < SPL; ++r) {
+                const int ss = lane + 32 * r;
+                mv[r] = ss < sb ? __ldcg(ml + ss * ml_stride) : -INFINITY;
+                lv[r] = ss < sb ? __ldcg(ml + ss * ml_stride + 1) : 0.f;
+                M = fmaxf(M, mv[r]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float Mr = M == -INFINITY ? 0.f : M;
+            float lt = 0.f;
+#pragma unroll
+            for (int r = 0; r < SPL; ++r) {
+                const int ss = lane + 32 * r;
+                if (ss < sb) {
+                    const float wt = ex2(mv[r] - Mr);
+                    s_w[ss * G + gg] = wt;
+                    lt += wt * lv[r];
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+            if (lane == 0) s_lt[gg] = lt;
+        }
+        __syncthreads();
+        float acc[EPT];
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) acc[k] = 0.f;
+        for (int ss = 0; ss < sb; ss += 8) {   // each element summed in split order
+            if (ss > 0) load8(ss);
+#pragma unroll
+            for (int k = 0; k < EPT; ++k) {
+                const int e = tid + k * kDecThreads;
+                if (e >= G * D) continue;
+                const int gg = e / D;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (ss + j < sb) acc[k] += s_w[(ss + j) * G + gg] * v[k][j];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int e = tid + k * kDecThreads;
+            if (e >= G * D) continue;
+            const float lt = s_lt[e / D];
+            a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc[k] / lt : 0.f);
+        }
+        if (tid == 0) a.counters[b * Hkv + h] = 0;
+        __syncthreads();
+    };
+    // examine the pending ticket (whole CTA): merge if this CTA was last
+    auto resolve_ticket = [&]() {
+        if (tid == 0) {
+            // the ticket's acquire made the other CTAs' partials visible
+            s_flag = pend_prev >= 0 && pend_prev == s_pend[2] - 1;
+            pend_prev = -1;
+        }
+        __syncthreads();
+        if (s_flag) merge_splits(s_pend[0], s_pend[1], s_pend[2]);
+    };
+
+    int n_done = 0;   // tiles computed by this warp
+    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+        const DecItem I = dec_item(a, s_pref, chunk, item);
+        const int hq0 = I.h * G;
+        // Q^T as the MMA's B operand: n = head (8 per n-tile), k = d
+        uint32_t qb[KSTEPS][NH][2];
+        {
+            const uint32_t *q32 = reinterpret_cast<const uint32_t *>(a.q + ((int64_t)I.b * a.Hq + hq0) * D);
+            // every load is issued before any use: q words first, then (fused
+            // step) the cos/sin values of this lane's pairs -- word i of a head
+            // row is RoPE pair i, rotated by table row positions[b]
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt) {
+                    const int hd = nt * 8 + g;
+                    qb[kk][nt][0] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + t4) : 0u;
+                    qb[kk][nt][1] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + 4 + t4) : 0u;
+                }
+            if (FUSED) {
+                const int k_item = (item - (int)blockIdx.x) / (int)gridDim.x;
+                const int32_t p = k_item < kDecThreads ? s_pos[k_item] : __ldg(a.positions + I.b);
+                const int32_t pc = (p >= 0 && p < a.max_pos) ? p : 0;   // out of range: no rotation (below)
+                const float *ct = a.cos_tab + (int64_t)pc * (D / 2), *sn = a.sin_tab + (int64_t)pc * (D / 2);
+                float cv[KSTEPS][2], sv[KSTEPS][2];
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    cv[kk][0] = __ldg(ct + kk * 8 + t4);
+                    cv[kk][1] = __ldg(ct + kk * 8 + 4 + t4);
+                    sv[kk][0] = __ldg(sn + kk * 8 + t4);
+                    sv[kk][1] = __ldg(sn + kk * 8 + 4 + t4);
+                }
+                if (pc == p) {
+#pragma unroll
+                    for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                        for (int nt = 0; nt < NH; ++nt) {
+                            qb[kk][nt][0] = rope_pair_bf16(qb[kk][nt][0], cv[kk][0], sv[kk][0]);
+                            qb[kk][nt][1] = rope_pair_bf16(qb[kk][nt][1], cv[kk][1], sv[kk][1]);
+                        }
+                }
+            }
+        }
+        float o[DM][NH][4];
+#pragma unroll
+        for (int i = 0; i < DM; ++i)
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) o[i][nt][0] = o[i][nt][1] = o[i][nt][2] = o[i][nt][3] = 0.f;
+        float m[NH][2], l[NH][2];
+#pragma unroll
+        for (int nt = 0; nt < NH; ++nt) m[nt][0] = m[nt][1] = -INFINITY, l[nt][0] = l[nt][1] = 0.f;
+
+        for (int i = warp; i < I.ntiles; i += kDecWarps) {
+            if (!bad) issue();
+            const int st = n_done % S;
+            if (!bad && !mbar_wait(bars + st * 8, (n_done / S) & 1, s_abort, a.err, PA_DEVERR_TIMEOUT)) bad = true;
+            ++n_done;
+            if (bad) continue;
+            const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile;
+            const uint32_t vmask = s_vmask[warp * S + st];
+            // S^T = K Q^T (16 tokens x 8 heads per n-tile)
+            float sc[NH][4], sc2[NH][4];   // two independent accumulation chains (even / odd k)
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) {
+                sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+                sc2[nt][0] = sc2[nt][1] = sc2[nt][2] = sc2[nt][3] = 0.f;
+            }
+            {
+                const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int c_hi = lane >> 4;
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    uint32_t af[4];
+                    ldmatrix_x4(kb + L::off(r, kk * 2 + c_hi), af[0], af[1], af[2], af[3]);
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt) {
+                        if (kk & 1) mma_bf16_16816(sc2[nt], af, qb[kk][nt][0], qb[kk][nt][1]);
+                        else mma_bf16_16816(sc[nt], af, qb[kk][nt][0], qb[kk][nt][1]);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[nt][e] += sc2[nt][e];
+            }
+            // mask, scale; column (head) maxima over the 16 tokens
+            const bool ok0 = (vmask >> g) & 1u, ok1 = (vmask >> (g + 8)) & 1u;
+            float mr[NH][2], al[NH][2];
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) {
+                sc[nt][0] = ok0 ? sc[nt][0] * a.scale_log2 : -INFINITY;
+                sc[nt][1] = ok0 ? sc[nt][1] * a.scale_log2 : -INFINITY;
+                sc[nt][2] = ok1 ? sc[nt][2] * a.scale_log2 : -INFINITY;
+                sc[nt][3] = ok1 ? sc[nt][3] * a.scale_log2 : -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    float v = fmaxf(sc[nt][j], sc[nt][j + 2]);
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+                    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+                    const float mn = fmaxf(m[nt][j], v);
+                    mr[nt][j] = mn == -INFINITY ? 0.f : mn;
+                    al[nt][j] = ex2(m[nt][j] - mr[nt][j]);
+                    m[nt][j] = mn;
+                }
+            }
+            // P = exp2(s - m), lane-partial column sums, P^T fragments
+            uint32_t pb[NH][2];
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) {
+                const float p0 = ex2(sc[nt][0] - mr[nt][0]);
+                const float p1 = ex2(sc[nt][1] - mr[nt][1]);
+                const float p2 = ex2(sc[nt][2] - mr[nt][0]);
+                const float p3 = ex2(sc[nt][3] - mr[nt][1]);
+                l[nt][0] = l[nt][0] * al[nt][0] + (p0 + p2);
+                l[nt][1] = l[nt][1] * al[nt][1] + (p1 + p3);
+                pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+                pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+            }
+#pragma unroll
+            for (int dm = 0; dm < DM; ++dm)
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt) {
+                    o[dm][nt][0] *= al[nt][0];
+                    o[dm][nt][1] *= al[nt][1];
+                    o[dm][nt][2] *= al[nt][0];
+                    o[dm][nt][3] *= al[nt][1];
+                }
+            // O^T += V^T P^T: V^T fragments by transposing ldmatrix of the V rows
+            {
+                const int r = ((lane >> 4) & 1) * 8 + (lane & 7);
+                const int c_lo = (lane >> 3) & 1;
+#pragma unroll
+                for (int dm = 0; dm < DM; ++dm) {
+                    uint32_t af[4];
+                    ldmatrix_x4_trans(vb + L::off(r, dm * 2 + c_lo), af[0], af[1], af[2], af[3]);
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt) mma_bf16_16816(o[dm][nt], af, pb[nt][0], pb[nt][1]);
+                }
+            }
+            __syncwarp();
+        }
+
+        // ------------------------------------- merge the warps' states
+#pragma unroll
+        for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 4);
+                l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 8);
+                l[nt][j] += __shfl_xor_sync(0xffffffffu, l[nt][j], 16);
+            }
+        // scratch free (the previous item is done with it); all warps stop
+        // together if any ring wait timed out
+        if (__syncthreads_or(bad)) break;
+        resolve_ticket();   // the previous item's split merge, if this CTA completed it
+        if (g == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int hd = nt * 8 + 2 * t4 + j;
+                    if (hd < G) {
+                        s_m[warp][hd] = m[nt][j];
+                        s_l[warp][hd] = l[nt][j];
+                    }
+                }
+        }
+        // O states go through the scratch in two rounds (warps 0-3, then 4-7);
+        // every element still sums warps 0..7 in order with the same weights
+        constexpr int EPT = (8 * NH * D + kDecThreads - 1) / kDecThreads;
+        float acc[EPT], lsum[EPT], Mx[EPT];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            if (rr == 1) __syncthreads();   // round 0 readers are done with the scratch
+            if ((warp >> 2) == rr) {
+                const int wl = warp & 3;
+#pragma unroll
+                for (int dm = 0; dm < DM; ++dm)
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int hd = nt * 8 + 2 * t4 + (e & 1);
+                            const int d = dm * 16 + g + 8 * (e >> 1);
+                            if (hd < G) scratch[(wl * G + hd) * D + d] = o[dm][nt][e];
+                        }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < EPT; ++k) {
+                const int e = tid + k * kDecThreads;
+                if (e >= G * D) continue;
+                const int gg = e / D, d = e - gg * D;
+                if (rr == 0) {
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, s_m[w][gg]);
+                    Mx[k] = M;
+                    acc[k] = 0.f;
+                    lsum[k] = 0.f;
+                }
+                const float Mr = Mx[k] == -INFINITY ? 0.f : Mx[k];
+#pragma unroll
+                for (int w = 0; w < kDecWarps / 2; ++w) {
+                    const int wg = rr * (kDecWarps / 2) + w;
+                    const float wt = ex2(s_m[wg][gg] - Mr);
+                    lsum[k] += wt * s_l[wg][gg];
+                    acc[k] += wt * scratch[(w * G + gg) * D + d];
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int e = tid + k * kDecThreads;
+            if (e >= G * D) continue;
+            const int gg = e / D, d = e - gg * D;
+            if (I.sb == 1) {
+                a.out[((int64_t)I.b * a.Hq + hq0 + gg) * D + d] =
+                    __float2bfloat16_rn(lsum[k] > 0.f ? acc[k] / lsum[k] : 0.f);
+            } else {
+                const int64_t pr = ((int64_t)I.s * a.cap_batch + I.b) * a.Hq + hq0 + gg;
+                a.o_part[pr * D + d] = acc[k];
+                if (d == 0) {
+                    a.ml_part[pr * 2] = Mx[k];
+                    a.ml_part[pr * 2 + 1] = lsum[k];
+                }
+            }
+        }
+        if (I.sb > 1) {
+            // ticket for (b, h): the barrier orders every thread's partial
+            // stores before thread 0's acquire-release atomic (release: this
+            // CTA's partials; acquire: those of the CTAs that came before, for
+            // the one that completes the count); its result is only examined at
+            // the next item end (or at exit), so the round trip overlaps the
+            // next item's tiles
+            __syncthreads();
+            if (tid == 0) {
+                pend_prev = atom_add_acq_rel_gpu(a.counters + I.b * Hkv + I.h, 1);
+                s_pend[0] = I.b;
+                s_pend[1] = I.h;
+                s_pend[2] = I.sb;
+            }
+        }
+    }
+    if (!bad && !*s_abort) resolve_ticket();
+    if (bad || *s_abort) {
+        // aborted: let this warp's loads already in flight land before the
+        // CTA's shared memory goes away (bounded, 10 ms per stage)
+        for (int j = n_done; j < n_issued; ++j) {
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(bars + (j % S) * 8, (j / S) & 1) && global_ns() - t0 < 10000000ull) {
+            }
+        }
+    }
+}
+
+template <int D, int S, int NH, bool FUSED>
+static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
+{
+    auto kern = paged_decode_kernel<D, S, NH, FUSED>;
+    const size_t smem = DecSmem<D, S, NH>::bytes(a.batch);
+    if (smem > kSmemLimit) return PA_ERR_UNSUPPORTED;
+    static size_t configured = 0;
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return PA_ERR_CUDA;
+        configured = smem;
+    }
+    if (launch_kernel(kern, dim3(num_sms()), dim3(kDecThreads), smem, st, a) != cudaSuccess) return PA_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Deepest ring whose shared memory fits this batch.
+template <int D, int NH, bool FUSED>
+static pa_status dispatch_decode(const DecodeArgs &a, cudaStream_t st)
+{
+    if (DecSmem<D, 4, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 4, NH, FUSED>(a, st);
+    if (DecSmem<D, 3, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 3, NH, FUSED>(a, st);
+    return launch_decode<D, 2, NH, FUSED>(a, st);
+}
+static_assert(DecSmem<128, 2, 2>::bytes(kDecMaxBatch) <= kSmemLimit, "decode smem at the largest batch");
+
+
+
+// Inputs of the fused step that a plain decode call does not have.
+struct StepInputs {
+    const void *k_new, *v_new;
+    const int32_t *positions, *loc;
+    const float *cos_tab, *sin_tab;
+    int max_pos;
+};
+
+template <bool FUSED>
+static pa_status decode_call(const void *q, int batch, int n_q_heads, const void *k_buf, const void *v_buf,
+                             pa_kv_shape s, int layer_id, const int32_t *req_to_token, int req_rows, int max_ctx,
+                             const int32_t *req_pool_indices, const int32_t *seq_lens, float scale, void *workspace,
+                             size_t workspace_bytes, int max_splits, void *out, const StepInputs *step,
+                             cudaStream_t st)
+{
+    if (batch < 0 || batch > kDecMaxBatch || n_q_heads <= 0 || s.n_layers <= 0 || s.size <= 0 ||
+        s.n_kv_heads <= 0 || req_rows <= 0 || max_ctx <= 0 || max_splits < 1 || max_splits > kDecMaxSplits)
+        return PA_ERR_SHAPE;
+    if (layer_id < 0 || layer_id >= s.n_layers) return PA_ERR_SHAPE;
+    if (n_q_heads % s.n_kv_heads != 0) return PA_ERR_SHAPE;
+    if (step && step->max_pos <= 0) return PA_ERR_SHAPE;
+    const int G = n_q_heads / s.n_kv_heads;
+    if (G > 16 || (s.head_dim != 64 && s.head_dim != 128)) return PA_ERR_UNSUPPORTED;
+    if (!workspace) return PA_ERR_NULL;
+    if (!aligned256(workspace)) return PA_ERR_ALIGN;
+    const DecodeWsLayout ws = decode_ws_layout(workspace_bytes, n_q_heads, s.n_kv_heads, s.head_dim, max_splits);
+    if (ws.cap_batch < batch || ws.total > workspace_bytes) return PA_ERR_WORKSPACE;
+    if (batch == 0) return PA_OK;
+    if (!q || !k_buf || !v_buf || !req_to_token || !req_pool_indices || !seq_lens || !out) return PA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_buf) || !aligned16(v_buf) || !aligned16(out) || !aligned4(req_to_token) ||
+        !aligned4(req_pool_indices) || !aligned4(seq_lens))
+        return PA_ERR_ALIGN;
+    if (step) {
+        if (!step->k_new || !step->v_new || !step->positions || !step->loc || !step->cos_tab || !step->sin_tab)
+            return PA_ERR_NULL;
+        if (!aligned16(step->k_new) || !aligned16(step->v_new) || !aligned4(step->positions) ||
+            !aligned4(step->loc) || !aligned16(step->cos_tab) || !aligned16(step->sin_tab))
+            return PA_ERR_ALIGN;
+    }
+
+    if ((int64_t)s.n_layers * s.size >= (int64_t)INT32_MAX - 16) return PA_ERR_SHAPE;
+    DecodeArgs a;
+    memset(&a, 0, sizeof a);
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)s.n_kv_heads * s.head_dim, (cuuint64_t)s.n_layers * s.size};
+        const cuuint64_t strides[1] = {(cuuint64_t)s.n_kv_heads * s.head_dim * 2};
+        const cuuint32_t box[2] = {64, kDecTile};
+        if (!encode_tmap_bf16(&a.tm_k, k_buf, 2, dims, strides, box) ||
+            !encode_tmap_bf16(&a.tm_v, v_buf, 2, dims, strides, box))
+            return PA_ERR_CUDA;
+    }
+    a.layer_row0 = layer_id * s.size;
+    const int64_t layer_off = (int64_t)layer_id * s.size * s.n_kv_heads * s.head_dim;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k_layer = static_cast<const __nv_bfloat16 *>(k_buf) + layer_off;
+    a.v_layer = static_cast<const __nv_bfloat16 *>(v_buf) + layer_off;
+    a.req_to_token = req_to_token;
+    a.req_pool_indices = req_pool_indices;
+    a.seq_lens = seq_lens;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    unsigned char *w = static_cast<unsigned char *>(workspace);
+    a.err = reinterpret_cast<int32_t *>(w);
+    a.counters = reinterpret_cast<int32_t *>(w + ws.counters_off);
+    a.ml_part = reinterpret_cast<float *>(w + ws.ml_off);
+    a.o_part = reinterpret_cast<float *>(w + ws.o_off);
+    a.batch = batch;
+    a.Hq = n_q_heads;
+    a.Hkv = s.n_kv_heads;
+    a.G = G;
+    a.size = s.size;
+    a.req_rows = req_rows;
+    a.max_ctx = max_ctx;
+    a.cap_batch = ws.cap_batch;
+    a.max_splits = max_splits;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    a.early_meta = launch_overlap() == PA_OVERLAP_EARLY_METADATA;
+    if (step) {
+        a.k_new = static_cast<const __nv_bfloat16 *>(step->k_new);
+        a.v_new = static_cast<const __nv_bfloat16 *>(step->v_new);
+        a.positions = step->positions;
+        a.loc = step->loc;
+        a.cos_tab = step->cos_tab;
+        a.sin_tab = step->sin_tab;
+        a.max_pos = step->max_pos;
+        a.k_layer_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(k_buf)) + layer_off;
+        a.v_layer_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(v_buf)) + layer_off;
+    }
+    if (s.head_dim == 128) return G > 8 ? dispatch_decode<128, 2, FUSED>(a, st) : dispatch_decode<128, 1, FUSED>(a, st);
+    return G > 8 ? dispatch_decode<64, 2, FUSED>(a, st) : dispatch_decode<64, 1, FUSED>(a, st);
+}
+
+}  // namespace pa

@@ -174,6 +174,12 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 }
 
 // ---------------------------------------------------------------- fences
+// Order this thread's generic-proxy global writes before later async-proxy
+// (TMA) reads of the same addresses.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -74,23 +74,9 @@ __global__ void __launch_bounds__(256) rope_kernel(uint4 *__restrict__ q, uint4 
         // pairs 4c .. 4c+3 of this head: table row p, columns 4c .. 4c+3
         const float4 cs = __ldg(cos_tab + (int64_t)p * head_chunks + c);
         const float4 sn = __ldg(sin_tab + (int64_t)p * head_chunks + c);
-        uint4 x = *ptr;
-        const float cc[4] = {cs.x, cs.y, cs.z, cs.w};
-        const float ss[4] = {sn.x, sn.y, sn.z, sn.w};
-        uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            __nv_bfloat162 pr = *reinterpret_cast<__nv_bfloat162 *>(&w[j]);
-            const float x0 = __low2float(pr), x1 = __high2float(pr);
-            // x0*c - x1*s and x0*s + x1*c with the second product split exactly
-            // into p + e (FMA remainder), so a cancelling sum keeps its low bits
-            const float p0 = x1 * ss[j], e0 = fmaf(x1, ss[j], -p0);
-            const float p1 = x1 * cc[j], e1 = fmaf(x1, cc[j], -p1);
-            const float y0 = fmaf(x0, cc[j], -p0) - e0;
-            const float y1 = fmaf(x0, ss[j], p1) + e1;
-            w[j] = pack_bf16x2(y0, y1);
-        }
-        *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+        const uint4 x = *ptr;
+        *ptr = make_uint4(rope_pair_bf16(x.x, cs.x, sn.x), rope_pair_bf16(x.y, cs.y, sn.y),
+                          rope_pair_bf16(x.z, cs.z, sn.z), rope_pair_bf16(x.w, cs.w, sn.w));
     }
 }
 

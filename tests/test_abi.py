@@ -118,3 +118,22 @@ def test_launch_overlap_mode_switch(lib):
         assert api.pa_get_launch_overlap() == api.OVERLAP_OFF   # a rejected mode changes nothing
     finally:
         api.pa_set_launch_overlap(api.OVERLAP_OFF)
+
+
+def test_decode_step_host_validation(lib):
+    P = ctypes.c_void_p
+    ws_bytes = api.pa_decode_workspace_bytes(1, 8, 2, 64, 4)
+
+    def call(**kw):
+        a = dict(q=FAKE, kn=FAKE, vn=FAKE, pos=FAKE, cos=FAKE, sin=FAKE, max_pos=64, loc=FAKE, ws=FAKE)
+        a.update(kw)
+        return lib.pa_decode_step(P(a["q"]), P(a["kn"]), P(a["vn"]), 1, 8, P(a["pos"]), P(a["cos"]), P(a["sin"]),
+                                  a["max_pos"], P(FAKE), P(FAKE), _shape(), 0, P(a["loc"]), P(FAKE), 1, 16, P(FAKE),
+                                  P(FAKE), 0.125, P(a["ws"]), ws_bytes, 4, P(FAKE), None)
+    assert call(kn=0) == 1
+    assert call(loc=0) == 1
+    assert call(cos=0) == 1
+    assert call(max_pos=0) == 2
+    assert call(vn=FAKE + 8) == 3                 # k_new / v_new must be 16-byte aligned
+    assert call(pos=FAKE + 2) == 3
+    assert call(ws=FAKE + 16) == 3

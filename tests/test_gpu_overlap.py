@@ -120,3 +120,47 @@ def test_prefill_chain_identical_across_modes():
                 assert torch.equal(_bits(o), r), f"graph, mode {mode}"
         words = ws.view(torch.int32)
         assert int(words[0]) == 0 and int(words[16]) == 0 and int(words[32]) == 0
+
+
+def test_fused_steps_back_to_back_identical_across_modes():
+    # two layers' fused steps sharing one workspace, eagerly and in a graph:
+    # the second step's early index reads overlap the first step's tail
+    st = W.make_decode_step(lens=[2000, 5, 900], n_q_heads=32, n_kv_heads=8, head_dim=128, n_layers=2,
+                            size=8192, page_size=16, seed=41, layer=0, max_ctx=4096, fill_layers=[0, 1],
+                            device="cuda")
+    B, Hq, D = st.q.shape
+    ws = api.alloc_workspace(api.pa_decode_workspace_bytes(B, Hq, 8, D, 64))
+    kb0, vb0 = st.kv.k_buf.clone(), st.kv.v_buf.clone()
+    ref = None
+    for mode in MODES:
+        api.pa_set_launch_overlap(mode)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        outs = [torch.zeros_like(st.q) for _ in range(2)]
+
+        def steps():
+            for layer, o in enumerate(outs):
+                api.pa_decode_step(st.q, st.k_new, st.v_new, st.positions, st.cos_tab, st.sin_tab, st.kv.k_buf,
+                                   st.kv.v_buf, layer, st.loc, st.kv.req_to_token, st.kv.req_pool_indices,
+                                   st.kv.seq_lens, st.scale, ws, 64, o, stream=s)
+        st.kv.k_buf.copy_(kb0)
+        st.kv.v_buf.copy_(vb0)
+        with torch.cuda.stream(s):
+            steps()
+        torch.cuda.synchronize()
+        got = [_bits(o) for o in outs] + [_bits(st.kv.k_buf), _bits(st.kv.v_buf)]
+        if ref is None:
+            ref = got
+        for g_, r in zip(got, ref):
+            assert torch.equal(g_, r), f"eager, mode {mode}"
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            steps()
+        for _ in range(3):
+            for o in outs:
+                o.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            for o, r in zip(outs, ref):
+                assert torch.equal(_bits(o), r), f"graph, mode {mode}"
+        assert api.pa_get_error(ws) == 0
