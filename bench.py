@@ -349,7 +349,7 @@ def run_ours(args, rank, world, local):
     dec_gbs = dec_bytes_tot / (dec_ms_tot * 1e-3) / 1e9
     traffic = NCU_TRAFFIC.get("decode")
     traffic_val = None
-    if traffic and traffic.get("sha") == src_sha("pa_decode.cu"):
+    if traffic and traffic.get("sha") == src_sha("pa_decode.cuh"):
         # DRAM bytes per launch scale with the K/V bytes streamed: the capture's
         # traffic / algorithmic ratio times this workload's algorithmic bytes
         traffic_val = round(traffic["ratio"] * dec_bytes_tot / len(SWEEP))
