@@ -444,6 +444,18 @@ def secondary_workloads(dev, peaks, s):
                           "peak_tflops": peaks["bf16_tflops"]}
     except api.PaError as e:
         res["prefill"] = {"unavailable": str(e)}
+    # dense prefill (no cached prefix, K/V straight from the packed new tokens) on the same prompts
+    try:
+        dflops = 4.0 * D * HQ * sum(n * (n + 1) / 2 for n in pb.new_lens)
+        dense = lambda: api.pa_dense_prefill_attn(pb.q, pb.k_new, pb.v_new, pb.qo_indptr, pb.scale, ws, out, stream=s)
+        dense()
+        torch.cuda.synchronize()
+        g = capture(dense, s)
+        ms = time_graph(g, 20, s)
+        res["prefill"]["dense_no_prefix"] = {"causal_tflop": round(dflops / 1e12, 4), "ms": round(ms, 4),
+                                             "tflops": round(dflops / (ms * 1e-3) / 1e12, 1)}
+    except api.PaError as e:
+        res["prefill"]["dense_no_prefix"] = {"unavailable": str(e)}
     g_rope = capture(lambda: api.pa_rope_packed(pb.q, pb.k_new, pb.positions, pb.cos_tab, pb.sin_tab,
                                                 stream=s), s)
     ms = time_graph(g_rope, 20, s)

@@ -275,6 +275,32 @@ pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_heads, cons
                                 const int32_t *req_pool_indices, float scale, void *workspace,
                                 size_t workspace_bytes, void *out, cudaStream_t st);
 
+/* As pa_paged_prefill_attn, and the same epilogue also writes each request's
+ * last row, out[qo_indptr[r+1] - 1], to last_out[r]: bf16 [n_reqs, n_q_heads,
+ * head_dim] (commit e58a728: select per-request final logits from cumulative
+ * query lengths).  A request with no rows leaves last_out[r] unwritten.
+ * last_out must be non-NULL and 16-byte aligned. */
+pa_status pa_paged_prefill_attn_last(const void *q, int n_tokens, int n_q_heads, const void *k_buf,
+                                     const void *v_buf, pa_kv_shape s, int layer_id,
+                                     const int32_t *qo_indptr, const int32_t *kv_indptr, int n_reqs,
+                                     const int32_t *req_to_token, int req_rows, int max_ctx,
+                                     const int32_t *req_pool_indices, float scale, void *workspace,
+                                     size_t workspace_bytes, void *out, void *last_out, cudaStream_t st);
+
+/* Dense prefill: prompts with no cached prefix, K/V read straight from the
+ * packed new tokens instead of through a page table (commit e58a728: prompts
+ * packed into one forward, rows addressed by cumulative query lengths).
+ * q, out: bf16 [n_tokens, n_q_heads, head_dim]; k, v: bf16 [n_tokens,
+ * n_kv_heads, head_dim], the new tokens' (rotated) K and V, packed by the same
+ * qo_indptr; query i of request r attends to tokens 0..i of request r.
+ * Gives the same bits as pa_paged_prefill_attn over a cache holding exactly
+ * these rows with no prefix.  last_out as in pa_paged_prefill_attn_last, or
+ * NULL.  Supported: head_dim 128, G in {1, 2, 4, 8, 16}, n_reqs <= 2048. */
+pa_status pa_dense_prefill_attn(const void *q, int n_tokens, int n_q_heads, const void *k, const void *v,
+                                int n_kv_heads, int head_dim, const int32_t *qo_indptr, int n_reqs, float scale,
+                                void *workspace, size_t workspace_bytes, void *out, void *last_out,
+                                cudaStream_t st);
+
 #ifdef __cplusplus
 }
 #endif

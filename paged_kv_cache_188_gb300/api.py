@@ -41,7 +41,8 @@ class KvShape(ctypes.Structure):
 EXPORTS = ["pa_status_string", "pa_decode_workspace_bytes", "pa_prefill_workspace_bytes",
            "pa_workspace_init", "pa_get_error", "pa_get_error_word", "pa_kv_store", "pa_rope_packed",
            "pa_paged_decode_attn", "pa_paged_prefill_attn", "pa_paged_decode_attn_noalloc",
-           "pa_set_launch_overlap", "pa_get_launch_overlap", "pa_decode_step"]
+           "pa_set_launch_overlap", "pa_get_launch_overlap", "pa_decode_step",
+           "pa_paged_prefill_attn_last", "pa_dense_prefill_attn"]
 
 _lib = None
 
@@ -75,6 +76,9 @@ def lib():
                                                P, P]
     L.pa_decode_step.argtypes = [P, P, P, i32, i32, P, P, P, i32, P, P, KvShape, i32, P, P, i32, i32, P, P, f32,
                                  P, sz, i32, P, P]
+    L.pa_paged_prefill_attn_last.argtypes = [P, i32, i32, P, P, KvShape, i32, P, P, i32, P, i32, i32, P, f32, P,
+                                             sz, P, P, P]
+    L.pa_dense_prefill_attn.argtypes = [P, i32, i32, P, P, i32, i32, P, i32, f32, P, sz, P, P, P]
     L.pa_set_launch_overlap.argtypes = [i32]
     L.pa_get_launch_overlap.argtypes = []
     for name in EXPORTS[3:]:
@@ -263,7 +267,9 @@ def pa_paged_decode_attn_noalloc(q, k_buf, v_buf, layer_id, req_to_token, req_po
 
 
 def pa_paged_prefill_attn(q, k_buf, v_buf, layer_id, qo_indptr, kv_indptr, req_to_token, req_pool_indices,
-                          scale, workspace, out, stream=None):
+                          scale, workspace, out, stream=None, last_out=None):
+    """Ragged causal prefill over the paged cache; with ``last_out`` ([R, Hq, D])
+    each request's last row is also gathered there by the same kernel."""
     s = _kv_shape(k_buf, v_buf)
     _need(q, torch.bfloat16, "q", 3)
     _need(out, torch.bfloat16, "out", 3)
@@ -276,7 +282,35 @@ def pa_paged_prefill_attn(q, k_buf, v_buf, layer_id, qo_indptr, kv_indptr, req_t
     R = qo_indptr.numel() - 1
     if out.shape != q.shape or D != s.head_dim or kv_indptr.numel() != R + 1 or req_pool_indices.numel() != R:
         raise ValueError("q/out [T, n_q_heads, head_dim], indptrs [R+1], req_pool_indices [R] expected")
-    _ok("pa_paged_prefill_attn", lib().pa_paged_prefill_attn(
-        _p(q), T, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(qo_indptr), _p(kv_indptr), R, _p(req_to_token),
-        req_to_token.shape[0], req_to_token.shape[1], _p(req_pool_indices), float(scale), _p(workspace),
-        workspace.numel(), _p(out), _stream(stream)))
+    args = [_p(q), T, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(qo_indptr), _p(kv_indptr), R, _p(req_to_token),
+            req_to_token.shape[0], req_to_token.shape[1], _p(req_pool_indices), float(scale), _p(workspace),
+            workspace.numel(), _p(out)]
+    if last_out is None:
+        _ok("pa_paged_prefill_attn", lib().pa_paged_prefill_attn(*args, _stream(stream)))
+    else:
+        _need(last_out, torch.bfloat16, "last_out", 3)
+        if last_out.shape != (R, Hq, D):
+            raise ValueError("last_out [R, n_q_heads, head_dim] expected")
+        _ok("pa_paged_prefill_attn_last", lib().pa_paged_prefill_attn_last(*args, _p(last_out), _stream(stream)))
+
+
+def pa_dense_prefill_attn(q, k, v, qo_indptr, scale, workspace, out, last_out=None, stream=None):
+    """Causal prefill of packed prompts with no cached prefix: K/V are the new
+    tokens' packed rows [T, Hkv, D], no page table."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k, torch.bfloat16, "k", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(qo_indptr, torch.int32, "qo_indptr", 1)
+    _need(workspace, torch.uint8, "workspace")
+    T, Hq, D = q.shape
+    R = qo_indptr.numel() - 1
+    if out.shape != q.shape or k.shape != v.shape or k.shape[0] != T or k.shape[2] != D:
+        raise ValueError("q/out [T, Hq, D], k/v [T, Hkv, D] expected")
+    if last_out is not None:
+        _need(last_out, torch.bfloat16, "last_out", 3)
+        if last_out.shape != (R, Hq, D):
+            raise ValueError("last_out [R, n_q_heads, head_dim] expected")
+    _ok("pa_dense_prefill_attn", lib().pa_dense_prefill_attn(
+        _p(q), T, Hq, _p(k), _p(v), k.shape[1], D, _p(qo_indptr), R, float(scale), _p(workspace), workspace.numel(),
+        _p(out), _p(last_out), _stream(stream)))

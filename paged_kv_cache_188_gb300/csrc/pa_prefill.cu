@@ -90,13 +90,14 @@ struct PrefillParams {
     int T, Hq, Hkv, G, TQ, R;
     int size, layer_row0, total_rows, req_rows, max_ctx;
     int early_meta;       // launched behind another kernel: plan before waiting for it
+    __nv_bfloat16 *last_out;   // optional [R, Hq, 128]: each request's last row of out
     float scale_log2;
 };
 
 struct alignas(16) PfItem {
     int h, qs, q0, nqa, nqb, p, row, n_keys, ntiles;   // q0: first token of tile A; nqb == 0: no tile B
     int end;                                           // 1: no more items for this CTA
-    int pad[2];
+    int r, nr;                                         // request and its number of new tokens
 };
 static_assert(kOffRing + kRing * (int)sizeof(PfItem) <= kOffMisc + 256, "item ring fits the misc area");
 
@@ -107,6 +108,7 @@ __device__ __forceinline__ float ex2f(float x)
     return y;
 }
 
+template <bool DENSE>
 __device__ __forceinline__ PfItem pf_item(const PrefillParams &p, const int *s_pref, int item)
 {
     int lo = 0, hi = p.R;   // largest r with s_pref[r] <= item
@@ -123,17 +125,20 @@ __device__ __forceinline__ PfItem pf_item(const PrefillParams &p, const int *s_p
     const int jp = pairs_r - 1 - jj;            // later (heavier) pairs first
     I.qs = __ldg(p.qo_indptr + r);
     const int n_r = __ldg(p.qo_indptr + r + 1) - I.qs;
-    const int L_r = __ldg(p.kv_indptr + r + 1) - __ldg(p.kv_indptr + r);
+    const int L_r = DENSE ? n_r : __ldg(p.kv_indptr + r + 1) - __ldg(p.kv_indptr + r);
     I.p = L_r - n_r;
+    I.r = r;
+    I.nr = n_r;
     I.q0 = 2 * jp * p.TQ;
     I.nqa = min(p.TQ, n_r - I.q0);
     I.nqb = max(0, min(p.TQ, n_r - I.q0 - p.TQ));
-    I.row = __ldg(p.req_pool_indices + r);
+    I.row = DENSE ? 0 : __ldg(p.req_pool_indices + r);
     I.n_keys = I.p + I.q0 + I.nqa + I.nqb;
     I.ntiles = (I.n_keys + kPfKeys - 1) / kPfKeys;
     return I;
 }
 
+template <bool DENSE, bool LAST>
 __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __grid_constant__ PrefillParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -181,8 +186,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
         auto pairs_of = [&](int r) -> int {
             const int qa = __ldg(p.qo_indptr + r), qb = __ldg(p.qo_indptr + r + 1);
             const int n_r = qb - qa;
-            const int L_r = __ldg(p.kv_indptr + r + 1) - __ldg(p.kv_indptr + r);
-            const int row = __ldg(p.req_pool_indices + r);
+            const int L_r = DENSE ? n_r : __ldg(p.kv_indptr + r + 1) - __ldg(p.kv_indptr + r);
+            const int row = DENSE ? 0 : __ldg(p.req_pool_indices + r);
             if (n_r <= 0) {
                 if (n_r < 0) pend_err |= PA_DEVERR_LEN;
                 return 0;
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
             item = __shfl_sync(0xffffffffu, item, 0);
             PfItem I;
             if (item < total_items) {
-                I = pf_item(p, s_pref, item);
+                I = pf_item<DENSE>(p, s_pref, item);
                 I.end = 0;
             } else {
                 I.end = 1;
@@ -262,7 +267,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 tma_load_3d(sQB, &p.tm_q, 0, I.h * G, I.qs + I.q0 + p.TQ, bar(Q_FULL));
                 tma_load_3d(sQB + kHalf, &p.tm_q, 64, I.h * G, I.qs + I.q0 + p.TQ, bar(Q_FULL));
             }
-            const int32_t *r2t = p.req_to_token + (int64_t)I.row * p.max_ctx;
+            const int32_t *r2t = DENSE ? nullptr : p.req_to_token + (int64_t)I.row * p.max_ctx;
+            // tensor-map row of slot / position 0: the layer's first slot, or
+            // (dense) the request's first packed token
+            const int row0 = DENSE ? I.qs : p.layer_row0;
             const int col0 = I.h * kPfD;
             const int gi = lane >> 2, sub = lane & 3;
             for (int t = 0; t < I.ntiles; ++t, ++kt) {
@@ -276,8 +284,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 for (int e = 0; e < 4; ++e) {
                     const int pos = k0 + 4 * lane + e;
                     okp[e] = pos < I.n_keys;
-                    slot[e] = okp[e] ? __ldg(r2t + pos) : -1;
-                    if (okp[e] && (slot[e] < 0 || slot[e] >= p.size)) {
+                    slot[e] = okp[e] ? (DENSE ? pos : __ldg(r2t + pos)) : -1;
+                    if (okp[e] && !DENSE && (slot[e] < 0 || slot[e] >= p.size)) {
                         set_error(err, PA_DEVERR_SLOT);
                         okp[e] = false;
                     }
@@ -293,7 +301,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                 auto issue = [&](const CUtensorMap *m16, const CUtensorMap *m1, uint32_t dst, uint32_t b) {
                     if (g_contig || g_empty) {
                         if (sub == 0) {
-                            const int row = g_empty ? p.total_rows : p.layer_row0 + s0;
+                            const int row = g_empty ? p.total_rows : row0 + s0;
                             tma_load_2d(dst + gi * 16 * 128, m16, col0, row, b);
                             tma_load_2d(dst + kHalf + gi * 16 * 128, m16, col0 + 64, row, b);
                         }
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int rr = 16 * gi + 4 * sub + e;
-                            const int row = okp[e] ? p.layer_row0 + slot[e] : p.total_rows;
+                            const int row = okp[e] ? row0 + slot[e] : p.total_rows;
                             tma_load_2d(dst + rr * 128, m1, col0, row, b);
                             tma_load_2d(dst + kHalf + rr * 128, m1, col0 + 64, row, b);
                         }
@@ -563,6 +571,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
                     if (ttok < nq) {
                         __nv_bfloat16 *dst = p.out + ((int64_t)(I.qs + q0 + ttok) * p.Hq + I.h * G + (trow - ttok * G)) * kPfD;
                         *reinterpret_cast<uint4 *>(dst + ch * 32 + cc * 8) = v;
+                        if (LAST && q0 + ttok == I.nr - 1) {   // the request's last row, gathered
+                            __nv_bfloat16 *lst = p.last_out + ((int64_t)I.r * p.Hq + I.h * G + (trow - ttok * G)) * kPfD;
+                            *reinterpret_cast<uint4 *>(lst + ch * 32 + cc * 8) = v;
+                        }
                     }
                 }
                 __syncwarp();
@@ -591,12 +603,85 @@ __global__ void __launch_bounds__(kPfThreads, 1) paged_prefill_kernel(const __gr
 
 using namespace pa;
 
-extern "C" pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_heads, const void *k_buf,
-                                           const void *v_buf, pa_kv_shape s, int layer_id,
-                                           const int32_t *qo_indptr, const int32_t *kv_indptr, int n_reqs,
-                                           const int32_t *req_to_token, int req_rows, int max_ctx,
-                                           const int32_t *req_pool_indices, float scale, void *workspace,
-                                           size_t workspace_bytes, void *out, cudaStream_t st)
+namespace pa {
+
+template <bool DENSE, bool LAST>
+static pa_status launch_prefill(const PrefillParams &prm, size_t smem, cudaStream_t st)
+{
+    auto kern = paged_prefill_kernel<DENSE, LAST>;
+    static size_t configured = 0;   // per instance
+    if (smem > configured) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return PA_ERR_CUDA;
+        configured = smem;
+    }
+    if (launch_kernel(kern, dim3(num_sms()), dim3(kPfThreads), smem, st, prm) != cudaSuccess) return PA_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Shared host path of the paged and dense entry points.  Paged: K/V rows are
+// slots of layer `layer_id` of [n_layers, size, Hkv, 128] buffers, reached
+// through req_to_token.  Dense: K/V are the packed new tokens' rows
+// [n_tokens, Hkv, 128] (no prefix: kv length = query length).
+static pa_status prefill_call(const void *q, int n_tokens, int n_q_heads, const void *k_rows, const void *v_rows,
+                              int n_kv_heads, int64_t total_rows, int layer_row0, int size,
+                              const int32_t *qo_indptr, const int32_t *kv_indptr, int n_reqs,
+                              const int32_t *req_to_token, int req_rows, int max_ctx,
+                              const int32_t *req_pool_indices, float scale, void *workspace, size_t workspace_bytes,
+                              void *out, void *last_out, bool dense, cudaStream_t st)
+{
+    PrefillParams prm;
+    memset(&prm, 0, sizeof prm);
+    const int G = n_q_heads / n_kv_heads;
+    const int TQ = kPfRows / G;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)kPfD, (cuuint64_t)n_q_heads, (cuuint64_t)n_tokens};
+        const cuuint64_t strides[2] = {(cuuint64_t)kPfD * 2, (cuuint64_t)n_q_heads * kPfD * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
+        if (!encode_tmap_bf16(&prm.tm_q, q, 3, dims, strides, box)) return PA_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)n_kv_heads * kPfD, (cuuint64_t)total_rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)n_kv_heads * kPfD * 2};
+        const cuuint32_t box16[2] = {64, 16}, box1[2] = {64, 1};
+        if (!encode_tmap_bf16(&prm.tm_k16, k_rows, 2, dims, strides, box16) ||
+            !encode_tmap_bf16(&prm.tm_k1, k_rows, 2, dims, strides, box1) ||
+            !encode_tmap_bf16(&prm.tm_v16, v_rows, 2, dims, strides, box16) ||
+            !encode_tmap_bf16(&prm.tm_v1, v_rows, 2, dims, strides, box1))
+            return PA_ERR_CUDA;
+    }
+    prm.qo_indptr = qo_indptr;
+    prm.kv_indptr = kv_indptr;
+    prm.req_to_token = req_to_token;
+    prm.req_pool_indices = req_pool_indices;
+    prm.out = static_cast<__nv_bfloat16 *>(out);
+    prm.last_out = static_cast<__nv_bfloat16 *>(last_out);
+    prm.err = static_cast<int32_t *>(workspace);
+    prm.queue = static_cast<int32_t *>(workspace) + kPrefillQueueWord;
+    prm.T = n_tokens;
+    prm.Hq = n_q_heads;
+    prm.Hkv = n_kv_heads;
+    prm.G = G;
+    prm.TQ = TQ;
+    prm.R = n_reqs;
+    prm.size = size;
+    prm.layer_row0 = layer_row0;
+    prm.total_rows = (int)total_rows;
+    prm.req_rows = req_rows;
+    prm.max_ctx = max_ctx;
+    prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    prm.early_meta = launch_overlap() == PA_OVERLAP_EARLY_METADATA;
+
+    const size_t smem = (size_t)kOffPref + (size_t)(n_reqs + 1) * 4 + 1024;
+    if (dense) return last_out ? launch_prefill<true, true>(prm, smem, st) : launch_prefill<true, false>(prm, smem, st);
+    return last_out ? launch_prefill<false, true>(prm, smem, st) : launch_prefill<false, false>(prm, smem, st);
+}
+
+static pa_status paged_call(const void *q, int n_tokens, int n_q_heads, const void *k_buf, const void *v_buf,
+                            pa_kv_shape s, int layer_id, const int32_t *qo_indptr, const int32_t *kv_indptr,
+                            int n_reqs, const int32_t *req_to_token, int req_rows, int max_ctx,
+                            const int32_t *req_pool_indices, float scale, void *workspace, size_t workspace_bytes,
+                            void *out, void *last_out, cudaStream_t st)
 {
     if (n_tokens < 0 || n_reqs < 0 || n_reqs > kPfMaxReqs || n_q_heads <= 0 || s.n_layers <= 0 || s.size <= 0 ||
         s.n_kv_heads <= 0 || req_rows <= 0 || max_ctx <= 0)
@@ -613,58 +698,58 @@ extern "C" pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_
     if (!q || !k_buf || !v_buf || !qo_indptr || !kv_indptr || !req_to_token || !req_pool_indices || !out)
         return PA_ERR_NULL;
     if (!aligned16(q) || !aligned16(k_buf) || !aligned16(v_buf) || !aligned16(out) || !aligned4(qo_indptr) ||
-        !aligned4(kv_indptr) || !aligned4(req_to_token) || !aligned4(req_pool_indices))
+        !aligned4(kv_indptr) || !aligned4(req_to_token) || !aligned4(req_pool_indices) ||
+        (last_out && !aligned16(last_out)))
         return PA_ERR_ALIGN;
+    return prefill_call(q, n_tokens, n_q_heads, k_buf, v_buf, s.n_kv_heads, (int64_t)s.n_layers * s.size,
+                        layer_id * s.size, s.size, qo_indptr, kv_indptr, n_reqs, req_to_token, req_rows, max_ctx,
+                        req_pool_indices, scale, workspace, workspace_bytes, out, last_out, false, st);
+}
 
-    PrefillParams prm;
-    memset(&prm, 0, sizeof prm);
-    const int TQ = kPfRows / G;
-    {
-        const cuuint64_t dims[3] = {(cuuint64_t)kPfD, (cuuint64_t)n_q_heads, (cuuint64_t)n_tokens};
-        const cuuint64_t strides[2] = {(cuuint64_t)kPfD * 2, (cuuint64_t)n_q_heads * kPfD * 2};
-        const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
-        if (!encode_tmap_bf16(&prm.tm_q, q, 3, dims, strides, box)) return PA_ERR_CUDA;
-    }
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)s.n_kv_heads * kPfD, (cuuint64_t)s.n_layers * s.size};
-        const cuuint64_t strides[1] = {(cuuint64_t)s.n_kv_heads * kPfD * 2};
-        const cuuint32_t box16[2] = {64, 16}, box1[2] = {64, 1};
-        if (!encode_tmap_bf16(&prm.tm_k16, k_buf, 2, dims, strides, box16) ||
-            !encode_tmap_bf16(&prm.tm_k1, k_buf, 2, dims, strides, box1) ||
-            !encode_tmap_bf16(&prm.tm_v16, v_buf, 2, dims, strides, box16) ||
-            !encode_tmap_bf16(&prm.tm_v1, v_buf, 2, dims, strides, box1))
-            return PA_ERR_CUDA;
-    }
-    prm.qo_indptr = qo_indptr;
-    prm.kv_indptr = kv_indptr;
-    prm.req_to_token = req_to_token;
-    prm.req_pool_indices = req_pool_indices;
-    prm.out = static_cast<__nv_bfloat16 *>(out);
-    prm.err = static_cast<int32_t *>(workspace);
-    prm.queue = static_cast<int32_t *>(workspace) + kPrefillQueueWord;
-    prm.T = n_tokens;
-    prm.Hq = n_q_heads;
-    prm.Hkv = s.n_kv_heads;
-    prm.G = G;
-    prm.TQ = TQ;
-    prm.R = n_reqs;
-    prm.size = s.size;
-    prm.layer_row0 = layer_id * s.size;
-    prm.total_rows = s.n_layers * s.size;
-    prm.req_rows = req_rows;
-    prm.max_ctx = max_ctx;
-    prm.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    prm.early_meta = launch_overlap() == PA_OVERLAP_EARLY_METADATA;
+}  // namespace pa
 
-    const size_t smem = (size_t)kOffPref + (size_t)(n_reqs + 1) * 4 + 1024;
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return PA_ERR_CUDA;
-        configured = smem;
-    }
-    if (launch_kernel(paged_prefill_kernel, dim3(num_sms()), dim3(kPfThreads), smem, st, prm) != cudaSuccess)
-        return PA_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+extern "C" pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_heads, const void *k_buf,
+                                           const void *v_buf, pa_kv_shape s, int layer_id,
+                                           const int32_t *qo_indptr, const int32_t *kv_indptr, int n_reqs,
+                                           const int32_t *req_to_token, int req_rows, int max_ctx,
+                                           const int32_t *req_pool_indices, float scale, void *workspace,
+                                           size_t workspace_bytes, void *out, cudaStream_t st)
+{
+    return paged_call(q, n_tokens, n_q_heads, k_buf, v_buf, s, layer_id, qo_indptr, kv_indptr, n_reqs, req_to_token,
+                      req_rows, max_ctx, req_pool_indices, scale, workspace, workspace_bytes, out, nullptr, st);
+}
+
+extern "C" pa_status pa_paged_prefill_attn_last(const void *q, int n_tokens, int n_q_heads, const void *k_buf,
+                                                const void *v_buf, pa_kv_shape s, int layer_id,
+                                                const int32_t *qo_indptr, const int32_t *kv_indptr, int n_reqs,
+                                                const int32_t *req_to_token, int req_rows, int max_ctx,
+                                                const int32_t *req_pool_indices, float scale, void *workspace,
+                                                size_t workspace_bytes, void *out, void *last_out, cudaStream_t st)
+{
+    if (!last_out && n_tokens > 0 && n_reqs > 0) return PA_ERR_NULL;
+    return paged_call(q, n_tokens, n_q_heads, k_buf, v_buf, s, layer_id, qo_indptr, kv_indptr, n_reqs, req_to_token,
+                      req_rows, max_ctx, req_pool_indices, scale, workspace, workspace_bytes, out, last_out, st);
+}
+
+extern "C" pa_status pa_dense_prefill_attn(const void *q, int n_tokens, int n_q_heads, const void *k, const void *v,
+                                           int n_kv_heads, int head_dim, const int32_t *qo_indptr, int n_reqs,
+                                           float scale, void *workspace, size_t workspace_bytes, void *out,
+                                           void *last_out, cudaStream_t st)
+{
+    if (n_tokens < 0 || n_reqs < 0 || n_reqs > kPfMaxReqs || n_q_heads <= 0 || n_kv_heads <= 0)
+        return PA_ERR_SHAPE;
+    if (n_q_heads % n_kv_heads != 0) return PA_ERR_SHAPE;
+    const int G = n_q_heads / n_kv_heads;
+    if (head_dim != kPfD || (G != 1 && G != 2 && G != 4 && G != 8 && G != 16)) return PA_ERR_UNSUPPORTED;
+    if (!workspace) return PA_ERR_NULL;
+    if (!aligned256(workspace)) return PA_ERR_ALIGN;
+    if (workspace_bytes < pa_prefill_workspace_bytes()) return PA_ERR_WORKSPACE;
+    if (n_tokens == 0 || n_reqs == 0) return PA_OK;
+    if (!q || !k || !v || !qo_indptr || !out) return PA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned4(qo_indptr) ||
+        (last_out && !aligned16(last_out)))
+        return PA_ERR_ALIGN;
+    // qo_indptr doubles as kv_indptr (kv length = query length); max_ctx bounds a request by the pack
+    return prefill_call(q, n_tokens, n_q_heads, k, v, n_kv_heads, n_tokens, 0, n_tokens, qo_indptr, qo_indptr, n_reqs,
+                        nullptr, 1, n_tokens, nullptr, scale, workspace, workspace_bytes, out, last_out, true, st);
 }

@@ -137,3 +137,18 @@ def test_decode_step_host_validation(lib):
     assert call(vn=FAKE + 8) == 3                 # k_new / v_new must be 16-byte aligned
     assert call(pos=FAKE + 2) == 3
     assert call(ws=FAKE + 16) == 3
+
+
+def test_prefill_variants_host_validation(lib):
+    P = ctypes.c_void_p
+    ws_bytes = api.pa_prefill_workspace_bytes()
+    rc = lib.pa_paged_prefill_attn_last(P(FAKE), 10, 8, P(FAKE), P(FAKE), api.KvShape(1, 64, 2, 128), 0, P(FAKE),
+                                        P(FAKE), 1, P(FAKE), 1, 16, P(FAKE), 0.1, P(FAKE), ws_bytes, P(FAKE), None, None)
+    assert rc == 1                                              # last_out is required
+    dense = lambda **kw: lib.pa_dense_prefill_attn(P(FAKE), 10, kw.get("hq", 8), P(FAKE), P(FAKE), kw.get("hkv", 2),
+                                                   kw.get("d", 128), P(FAKE), 1, 0.1, P(kw.get("ws", FAKE)), ws_bytes,
+                                                   P(FAKE), P(kw.get("last", 0)), None)
+    assert dense(d=64) == 4
+    assert dense(hq=6, hkv=4) == 2
+    assert dense(ws=0) == 1
+    assert dense(last=FAKE + 8) == 3

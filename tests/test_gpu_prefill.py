@@ -150,3 +150,40 @@ def test_config4_full_size_sampled():
                          npy(pb.kv.req_pool_indices), pb.scale, sel=(st, sh))
     got = npy(out.float())[st, sh]
     assert_attention_close(got, ref, "config 4 sampled")
+
+
+def test_last_rows_gathered_by_the_epilogue():
+    new, pre = [1, 31, 200, 64, 129], [0, 40, 300, 0, 17]
+    pb = W.make_prefill_batch(new_lens=new, prefix_lens=pre, n_q_heads=32, n_kv_heads=8, head_dim=128, size=8192,
+                              page_size=16, seed=21, device="cuda")
+    _store(pb)
+    ws = api.alloc_workspace(api.pa_prefill_workspace_bytes())
+    R = len(new)
+    out = torch.full_like(pb.q, float("nan"))
+    last = torch.full((R,) + tuple(pb.q.shape[1:]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    api.pa_paged_prefill_attn(pb.q, pb.kv.k_buf, pb.kv.v_buf, 0, pb.qo_indptr, pb.kv_indptr, pb.kv.req_to_token,
+                              pb.kv.req_pool_indices, pb.scale, ws, out, last_out=last)
+    ref, _ = _run(pb)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))    # the gather changes nothing else
+    rows = (pb.qo_indptr[1:] - 1).long()
+    assert torch.equal(last.view(torch.int16), ref[rows].view(torch.int16))
+    assert api.pa_get_error(ws) == 0
+
+
+@pytest.mark.parametrize("G", [1, 4, 16])
+def test_dense_prefill_equals_paged_prefill_without_prefix(G):
+    new = [1, 17, 300, 128, 1000, 65]
+    pb = W.make_prefill_batch(new_lens=new, prefix_lens=[0] * len(new), n_q_heads=2 * G, n_kv_heads=2,
+                              head_dim=128, size=4096, page_size=16, seed=30 + G, device="cuda")
+    kb, vb = _store(pb)
+    ref, _ = _run(pb)
+    ws = api.alloc_workspace(api.pa_prefill_workspace_bytes())
+    out = torch.full_like(pb.q, float("nan"))
+    last = torch.full((len(new),) + tuple(pb.q.shape[1:]), float("nan"), dtype=torch.bfloat16, device="cuda")
+    api.pa_dense_prefill_attn(pb.q, pb.k_new, pb.v_new, pb.qo_indptr, pb.scale, ws, out, last_out=last)
+    torch.cuda.synchronize()
+    assert api.pa_get_error(ws) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(last.view(torch.int16), ref[(pb.qo_indptr[1:] - 1).long()].view(torch.int16))
+    assert_attention_close(npy(out.float()), _ref(pb, kb, vb), f"dense prefill G={G}")
