@@ -506,6 +506,26 @@ def secondary_workloads(dev, peaks, s):
                      "decode_gbs_unique": round(unique / (ms_dec * 1e-3) / 1e9, 1),
                      "decode_gbs_logical": round(logical / (ms_dec * 1e-3) / 1e9, 1),
                      "frac_of_hbm_unique": round(unique / (ms_dec * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        if shared:
+            # cascade decode: each group's shared prefix read once per chunk of members
+            indptr, reqs, prefix = W.prefix_groups(lens, 8, 1024, 16)
+            n_groups = indptr.numel() - 1
+            caps = (B, n_groups, 8, MAX_SPLITS)
+            wsc = api.alloc_workspace(api.pa_cascade_workspace_bytes(*caps, Hq, HKV, D), dev)
+            ip, rq, px = indptr.to(dev), reqs.to(dev), prefix.to(dev)
+
+            def cascade():
+                api.pa_paged_decode_attn_cascade(q, st.kv.k_buf, st.kv.v_buf, 0, st.kv.req_to_token,
+                                                 st.kv.req_pool_indices, st.kv.seq_lens, ip, rq, px, st.scale, wsc,
+                                                 caps, out, stream=s)
+            cascade()
+            torch.cuda.synchronize()
+            g_c = capture(cascade, s)
+            ms_c = time_graph(g_c, 20, s)
+            res[name]["cascade_decode_us"] = round(ms_c * 1e3, 2)
+            res[name]["cascade_gbs_unique"] = round(unique / (ms_c * 1e-3) / 1e9, 1)
+            res[name]["cascade_frac_of_hbm_unique"] = round(unique / (ms_c * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+            del wsc, g_c
         del st, ws, out, q, kn, g_all, g_dec
         torch.cuda.empty_cache()
 

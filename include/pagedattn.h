@@ -253,6 +253,38 @@ pa_status pa_decode_step(const void *q, const void *k_new, const void *v_new, in
                          const int32_t *req_pool_indices, const int32_t *seq_lens, float scale,
                          void *workspace, size_t workspace_bytes, int max_splits, void *out, cudaStream_t st);
 
+/* ------------------------------------------------------- cascade decode
+ * Shared-prefix decode (commit 398e8a3 / e58a728: requests whose page-table
+ * rows point at the same cached prefix pages, radix reuse).  The members of
+ * group g are the requests group_reqs[group_indptr[g] .. group_indptr[g+1]),
+ * and the first group_prefix[g] tokens of every member sit on the same slots
+ * (the caller's contract; each member is in at most one group and
+ * group_prefix[g] < its seq_len).  Same result as pa_paged_decode_attn, within
+ * the attention tolerance (the split structure differs): the prefix is read
+ * once per chunk of 16 / G members, its rows merged with each member's own
+ * tokens by log-sum-exp.  Two kernel launches.
+ *   group_indptr int32 [n_groups + 1], group_reqs int32 [group_indptr[n_groups]],
+ *   group_prefix int32 [n_groups] (device); members past max_group_size in a
+ *   group are treated as ungrouped.
+ * The workspace layout is fixed by `caps`, which must be the same for every
+ * call on one workspace (sized by pa_cascade_workspace_bytes, initialised by
+ * pa_workspace_init); batch <= caps.max_batch, n_groups <= caps.max_groups,
+ * caps.max_groups * ceil(max_group_size / (16 / G)) <= 4096.  Other limits as
+ * pa_paged_decode_attn.  Under PA_OVERLAP_EARLY_METADATA the group arrays
+ * count as index inputs. */
+typedef struct {
+    int max_batch, max_groups, max_group_size, max_splits;
+} pa_cascade_caps;
+size_t pa_cascade_workspace_bytes(pa_cascade_caps caps, int n_q_heads, int n_kv_heads, int head_dim);
+pa_status pa_paged_decode_attn_cascade(const void *q, int batch, int n_q_heads, const void *k_buf,
+                                       const void *v_buf, pa_kv_shape s, int layer_id,
+                                       const int32_t *req_to_token, int req_rows, int max_ctx,
+                                       const int32_t *req_pool_indices, const int32_t *seq_lens,
+                                       const int32_t *group_indptr, const int32_t *group_reqs,
+                                       const int32_t *group_prefix, int n_groups, pa_cascade_caps caps,
+                                       float scale, void *workspace, size_t workspace_bytes, void *out,
+                                       cudaStream_t st);
+
 /* ----------------------------------------------------------- prefill attn
  * Commit e58a728: packed prompts with a shared prefix start in one forward,
  * paged prefill (attn_paged_prefill), rows located by cumulative query lengths;

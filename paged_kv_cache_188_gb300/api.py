@@ -33,6 +33,11 @@ class PaError(RuntimeError):
         super().__init__(f"{fn} returned {STATUS.get(status, status)}")
 
 
+class CascadeCaps(ctypes.Structure):
+    _fields_ = [("max_batch", ctypes.c_int), ("max_groups", ctypes.c_int), ("max_group_size", ctypes.c_int),
+                ("max_splits", ctypes.c_int)]
+
+
 class KvShape(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int), ("size", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int)]
@@ -42,7 +47,8 @@ EXPORTS = ["pa_status_string", "pa_decode_workspace_bytes", "pa_prefill_workspac
            "pa_workspace_init", "pa_get_error", "pa_get_error_word", "pa_kv_store", "pa_rope_packed",
            "pa_paged_decode_attn", "pa_paged_prefill_attn", "pa_paged_decode_attn_noalloc",
            "pa_set_launch_overlap", "pa_get_launch_overlap", "pa_decode_step",
-           "pa_paged_prefill_attn_last", "pa_dense_prefill_attn"]
+           "pa_paged_prefill_attn_last", "pa_dense_prefill_attn", "pa_cascade_workspace_bytes",
+           "pa_paged_decode_attn_cascade"]
 
 _lib = None
 
@@ -79,10 +85,14 @@ def lib():
     L.pa_paged_prefill_attn_last.argtypes = [P, i32, i32, P, P, KvShape, i32, P, P, i32, P, i32, i32, P, f32, P,
                                              sz, P, P, P]
     L.pa_dense_prefill_attn.argtypes = [P, i32, i32, P, P, i32, i32, P, i32, f32, P, sz, P, P, P]
+    L.pa_cascade_workspace_bytes.argtypes = [CascadeCaps, i32, i32, i32]
+    L.pa_paged_decode_attn_cascade.argtypes = [P, i32, i32, P, P, KvShape, i32, P, i32, i32, P, P, P, P, P, i32,
+                                               CascadeCaps, f32, P, sz, P, P]
     L.pa_set_launch_overlap.argtypes = [i32]
     L.pa_get_launch_overlap.argtypes = []
     for name in EXPORTS[3:]:
         getattr(L, name).restype = i32
+    L.pa_cascade_workspace_bytes.restype = sz
     _lib = L
     return L
 
@@ -314,3 +324,32 @@ def pa_dense_prefill_attn(q, k, v, qo_indptr, scale, workspace, out, last_out=No
     _ok("pa_dense_prefill_attn", lib().pa_dense_prefill_attn(
         _p(q), T, Hq, _p(k), _p(v), k.shape[1], D, _p(qo_indptr), R, float(scale), _p(workspace), workspace.numel(),
         _p(out), _p(last_out), _stream(stream)))
+
+
+def pa_cascade_workspace_bytes(max_batch, max_groups, max_group_size, max_splits, n_q_heads, n_kv_heads, head_dim):
+    return int(lib().pa_cascade_workspace_bytes(CascadeCaps(max_batch, max_groups, max_group_size, max_splits),
+                                                n_q_heads, n_kv_heads, head_dim))
+
+
+def pa_paged_decode_attn_cascade(q, k_buf, v_buf, layer_id, req_to_token, req_pool_indices, seq_lens, group_indptr,
+                                 group_reqs, group_prefix, scale, workspace, caps, out, stream=None):
+    """Decode attention with shared prefixes read once per chunk of group members.
+
+    ``caps`` = (max_batch, max_groups, max_group_size, max_splits): the same for
+    every call on one workspace (it fixes the workspace layout)."""
+    s = _kv_shape(k_buf, v_buf)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    for t, n in ((req_to_token, "req_to_token"), (req_pool_indices, "req_pool_indices"), (seq_lens, "seq_lens"),
+                 (group_indptr, "group_indptr"), (group_reqs, "group_reqs"), (group_prefix, "group_prefix")):
+        _need(t, torch.int32, n)
+    _need(workspace, torch.uint8, "workspace")
+    B, Hq, D = q.shape
+    n_groups = group_indptr.numel() - 1
+    if out.shape != q.shape or D != s.head_dim or group_prefix.numel() != n_groups:
+        raise ValueError("q/out [batch, Hq, D], group_indptr [n_groups + 1], group_prefix [n_groups] expected")
+    _ok("pa_paged_decode_attn_cascade", lib().pa_paged_decode_attn_cascade(
+        _p(q), B, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(req_to_token), req_to_token.shape[0],
+        req_to_token.shape[1], _p(req_pool_indices), _p(seq_lens), _p(group_indptr), _p(group_reqs),
+        _p(group_prefix), n_groups, CascadeCaps(*caps), float(scale), _p(workspace), workspace.numel(), _p(out),
+        _stream(stream)))

@@ -12,7 +12,7 @@ extern "C" pa_status pa_paged_decode_attn(const void *q, int batch, int n_q_head
                                           void *workspace, size_t workspace_bytes, int max_splits, void *out,
                                           cudaStream_t st)
 {
-    return decode_call<false>(q, batch, n_q_heads, k_buf, v_buf, s, layer_id, req_to_token, req_rows, max_ctx,
+    return decode_call<MODE_PLAIN>(q, batch, n_q_heads, k_buf, v_buf, s, layer_id, req_to_token, req_rows, max_ctx,
                        req_pool_indices, seq_lens, scale, workspace, workspace_bytes, max_splits, out, nullptr, st);
 }
 

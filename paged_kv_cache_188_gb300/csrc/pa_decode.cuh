@@ -68,6 +68,15 @@ constexpr int kDecMaxChunk = 1024;
 constexpr int kDecMaxBatch = 4096;
 constexpr int kDecMaxSplits = 128;
 
+// Kernel modes.  PLAIN: decode attention.  FUSED: the decode step (RoPE +
+// KV store + attention).  PREFIX / SUFFIX: the two launches of cascade
+// decode -- PREFIX runs "virtual requests" (a group's shared prefix against
+// the q rows of up to 16 / G members at once) and writes each row's
+// normalised output and log-sum-exp; SUFFIX runs every request over its
+// tokens after its group's prefix and folds the prefix result into its
+// output by log-sum-exp.
+enum DecMode { MODE_PLAIN = 0, MODE_FUSED = 1, MODE_PREFIX = 2, MODE_SUFFIX = 3 };
+
 struct DecodeArgs {
     CUtensorMap tm_k;    // 2-D (element, row) over k_buf rows, 64 x 16 boxes, 128-byte swizzle
     CUtensorMap tm_v;
@@ -99,6 +108,16 @@ struct DecodeArgs {
     __nv_bfloat16 *k_layer_w;   // the layer's K / V rows, writable
     __nv_bfloat16 *v_layer_w;
     int max_pos;
+    // cascade (PREFIX / SUFFIX)
+    const int32_t *grp_indptr;  // [n_groups + 1]: members of group g are grp_reqs[grp_indptr[g] ..)
+    const int32_t *grp_reqs;
+    const int32_t *grp_prefix;  // [n_groups]: tokens shared by every member
+    int n_groups, cpg, C;       // chunks per group, members per chunk (virtual request = (group, chunk))
+    int G_real, Hq_real, B_real;
+    int32_t *req_start;         // [B_real]: first token of the request's own part (PREFIX writes, SUFFIX reads)
+    int32_t *req_pre;           // [B_real]: virtual request * 16 + member slot, or -1
+    float *pre_o;               // [virtual batch, Hkv * G_v, D]: normalised prefix outputs
+    float *pre_lse;             // [virtual batch, Hkv * G_v]: their log2-sum-exp (scaled-score units)
 };
 
 __device__ __forceinline__ int clamp_len(int n, int max_ctx) { return n < 0 ? 0 : (n > max_ctx ? max_ctx : n); }
@@ -155,7 +174,7 @@ struct DecSmem {
     // half the warps' O states [4][G][D] fp32 at a time, later the split merge
     // [sb][G][2] + [sb][G] + [G]
     static constexpr int kCombine = (kDecWarps / 2) * 8 * NH * D * 4;
-    static constexpr int kMerge = (3 * kDecMaxSplits * 8 * NH + 8 * NH) * 4;
+    static constexpr int kMerge = (3 * kDecMaxSplits * 8 * NH + 16 * NH) * 4;
     static constexpr int kScratch = kCombine > kMerge ? kCombine : kMerge;
     static constexpr int kMaskOff = kScratchOff + kScratch;
     static constexpr int kBarOff = kMaskOff + kDecWarps * S * 4;
@@ -186,6 +205,46 @@ __device__ __forceinline__ int item_request(const int *s_pref, int batch, int it
     return lo;
 }
 
+// Tokens of request b this launch attends to: [start, start + n).  PREFIX:
+// a virtual request (group, chunk) covers its group's shared prefix (none for
+// an empty chunk) through the chunk's first member's page-table row.
+template <int MODE>
+__device__ __forceinline__ void req_span(const DecodeArgs &a, int b, int &start, int &n, int &row)
+{
+    if (MODE == MODE_PREFIX) {
+        const int g = b / a.cpg, c = b - g * a.cpg;
+        const int first = __ldg(a.grp_indptr + g) + c * a.C;
+        start = 0;
+        n = 0;
+        row = -1;
+        if (first < __ldg(a.grp_indptr + g + 1)) {
+            const int m0 = __ldg(a.grp_reqs + first);
+            if (m0 >= 0 && m0 < a.B_real) {
+                n = clamp_len(__ldg(a.grp_prefix + g), a.max_ctx);
+                row = __ldg(a.req_pool_indices + m0);
+            }
+        }
+        return;
+    }
+    const int full = clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
+    start = MODE == MODE_SUFFIX ? min(max(__ldg(a.req_start + b), 0), full) : 0;
+    n = full - start;
+    row = __ldg(a.req_pool_indices + b);
+}
+
+template <int MODE>
+__device__ __forceinline__ int req_len(const DecodeArgs &a, int b)
+{
+    if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED) {
+        return clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
+    } else {
+        int start, n, row;
+        req_span<MODE>(a, b, start, n, row);
+        return n;
+    }
+}
+
+template <int MODE>
 __device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pref, const DecPlan &chunk, int item)
 {
     const int lo = item_request(s_pref, a.batch, item);
@@ -194,24 +253,41 @@ __device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pr
     const int local = item - s_pref[lo];
     I.s = local / a.Hkv;
     I.h = local - I.s * a.Hkv;
-    int n = clamp_len(__ldg(a.seq_lens + lo), a.max_ctx);
-    int len;
-    split_of(n, chunk, a.max_splits, I.sb, len);
-    I.row = __ldg(a.req_pool_indices + lo);
-    if (I.row < 0 || I.row >= a.req_rows) {
-        I.row = -1;
-        n = 0;
+    if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED) {
+        int n = clamp_len(__ldg(a.seq_lens + lo), a.max_ctx);
+        int len;
+        split_of(n, chunk, a.max_splits, I.sb, len);
+        I.row = __ldg(a.req_pool_indices + lo);
+        if (I.row < 0 || I.row >= a.req_rows) {
+            I.row = -1;
+            n = 0;
+        }
+        I.t0 = I.s * len;
+        I.t1 = min(n, I.t0 + len);
+    } else {
+        int start, n;
+        req_span<MODE>(a, lo, start, n, I.row);
+        int len;
+        split_of(n, chunk, a.max_splits, I.sb, len);
+        if (I.row < 0 || I.row >= a.req_rows) {
+            I.row = -1;
+            n = 0;
+        }
+        I.t0 = start + I.s * len;
+        I.t1 = start + min(n, I.s * len + len);
     }
-    I.t0 = I.s * len;
-    I.t1 = min(n, I.t0 + len);
     I.ntiles = I.t1 > I.t0 ? (I.t1 - I.t0 + kDecTile - 1) / kDecTile : 0;
     return I;
 }
 
-template <int D, int S, int NH, bool FUSED>
+template <int D, int S, int NH, int MODE>
 __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __grid_constant__ DecodeArgs a)
 {
     using L = DecSmem<D, S, NH>;
+    constexpr bool FUSED = MODE == MODE_FUSED;
+    // the suffix launch plans from req_start, which the prefix launch writes:
+    // it never plans before its wait
+    const bool early = a.early_meta && MODE != MODE_SUFFIX;
     constexpr int KSTEPS = D / 16;
     constexpr int DM = D / 16;         // 16-row d tiles of O^T
     constexpr int CPR = D / 8;         // 16-byte chunks per row
@@ -240,11 +316,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         fence_mbar_init();
     }
     if (tid == 0) *s_abort = 0;
-    if (!a.early_meta) pdl_wait();
+    if (!early) pdl_wait();
 
     // ---------------------------------------------------------- planning
     int my_tot = 0;
-    for (int b = tid; b < B; b += kDecThreads) my_tot += clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
+    for (int b = tid; b < B; b += kDecThreads) my_tot += req_len<MODE>(a, b);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) my_tot += __shfl_xor_sync(0xffffffffu, my_tot, o);
     if (lane == 0) s_red[warp] = my_tot;
@@ -265,7 +341,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         int run = 0;
         for (int b = b_lo; b < b_hi; ++b) {
             int sb, len;
-            split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), chunk, a.max_splits, sb, len);
+            split_of(req_len<MODE>(a, b), chunk, a.max_splits, sb, len);
             run += sb * Hkv;
         }
         int incl = run;
@@ -283,7 +359,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         for (int b = b_lo; b < b_hi; ++b) {
             s_pref[b] = excl;
             int sb, len;
-            split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), chunk, a.max_splits, sb, len);
+            split_of(req_len<MODE>(a, b), chunk, a.max_splits, sb, len);
             excl += sb * Hkv;
         }
         if (tid == kDecThreads - 1) s_pref[B] = base + incl;
@@ -307,7 +383,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         while (c.item < total_items && c.tile >= c.I.ntiles) {
             c.item += gridDim.x;
             c.tile = warp;
-            if (c.item < total_items) c.I = dec_item(a, s_pref, chunk, c.item);
+            if (c.item < total_items) c.I = dec_item<MODE>(a, s_pref, chunk, c.item);
         }
         c.slot = -1;
         if (c.item < total_items && lane < kDecTile && c.I.row >= 0) {
@@ -321,7 +397,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     cur.I.ntiles = 0;
     cur.I.row = -1;
     cur.I.t0 = cur.I.t1 = cur.I.h = 0;
-    if (cur.item < total_items) cur.I = dec_item(a, s_pref, chunk, cur.item);
+    if (cur.item < total_items) cur.I = dec_item<MODE>(a, s_pref, chunk, cur.item);
     settle(cur);
     Cursor nxt = cur;
     nxt.tile += kDecWarps;
@@ -397,7 +473,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         const int first = blockIdx.x + pass * kDecThreads * (int)gridDim.x;
         const int item = first + tid * (int)gridDim.x;
         if (item < total_items) {
-            const DecItem I = dec_item(a, s_pref, chunk, item);
+            const DecItem I = dec_item<MODE>(a, s_pref, chunk, item);
             const int32_t p = __ldg(a.positions + I.b);
             if (pass == 0) s_pos[tid] = p;   // the q rotation of item tid needs no global load later
             if (I.s == I.sb - 1) {
@@ -433,8 +509,30 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     };
     bool more_steps = false;
     if (FUSED) more_steps = collect(0);
-    if (a.early_meta) pdl_wait();
+    if (early) pdl_wait();
     pdl_launch_dependents();
+    if (MODE == MODE_PREFIX && blockIdx.x == 0) {
+        // the suffix launch's per-request start token and prefix row
+        for (int b = tid; b < a.B_real; b += kDecThreads) {
+            a.req_start[b] = 0;
+            a.req_pre[b] = -1;
+        }
+        __syncthreads();
+        const int n_mem = __ldg(a.grp_indptr + a.n_groups);
+        for (int e = tid; e < n_mem; e += kDecThreads) {
+            int lo = 0, hi = a.n_groups;   // group of entry e: largest g with grp_indptr[g] <= e
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(a.grp_indptr + mid) <= e) lo = mid; else hi = mid;
+            }
+            const int i = e - __ldg(a.grp_indptr + lo);
+            const int b = __ldg(a.grp_reqs + e);
+            if (b >= 0 && b < a.B_real && i < a.cpg * a.C) {
+                a.req_start[b] = max(__ldg(a.grp_prefix + lo), 0);
+                a.req_pre[b] = (lo * a.cpg + i / a.C) * 16 + i % a.C;
+            }
+        }
+    }
     if (FUSED) {
         for (int pass = 1; more_steps; ++pass) {
             store_rows();
@@ -456,10 +554,39 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     // weights are computed warp-parallel (a warp per q head, lanes over
     // splits, shuffle max and sum).
     int pend_prev = -1;                        // thread 0: pending ticket result
+    // Final output of element (request b, q head hq, dim d) from the merged
+    // unnormalised acc, sum l and max mx (log2 units).  PREFIX writes the
+    // normalised fp32 row and its log-sum-exp; SUFFIX combines with the
+    // request's prefix row, if it has one, by log-sum-exp.
+    auto emit = [&](int b, int hq, int d, float acc, float l, float mx, int pre) {
+        const float o = l > 0.f ? acc / l : 0.f;
+        if (MODE == MODE_PREFIX) {
+            a.pre_o[((int64_t)b * a.Hq + hq) * D + d] = o;
+            if (d == 0) a.pre_lse[(int64_t)b * a.Hq + hq] = l > 0.f ? mx + __log2f(l) : -INFINITY;
+            return;
+        }
+        if (MODE == MODE_SUFFIX && pre >= 0) {
+            const int h = hq / G, j = hq - h * G;
+            const int64_t prow = ((int64_t)(pre >> 4) * Hkv + h) * (a.C * G) + (pre & 15) * G + j;
+            const float lse_p = __ldcg(a.pre_lse + prow), o_p = __ldcg(a.pre_o + prow * D + d);
+            const float lse_s = l > 0.f ? mx + __log2f(l) : -INFINITY;
+            const float M = fmaxf(lse_s, lse_p);
+            float val = 0.f;
+            if (M != -INFINITY) {
+                const float ws = ex2(lse_s - M), wp = ex2(lse_p - M);
+                val = (ws * o + wp * o_p) / (ws + wp);
+            }
+            a.out[((int64_t)b * a.Hq + hq) * D + d] = __float2bfloat16_rn(val);
+            return;
+        }
+        a.out[((int64_t)b * a.Hq + hq) * D + d] = __float2bfloat16_rn(o);
+    };
     auto merge_splits = [&](int b, int h, int sb) {
         const int hq0 = h * G;
         float *s_w = scratch;              // [sb][G] split weights
         float *s_lt = s_w + sb * G;        // [G] weighted sums of l
+        float *s_M = s_lt + G;             // [G] the maxima they are relative to
+        const int pre = MODE == MODE_SUFFIX ? __ldcg(a.req_pre + b) : -1;
         constexpr int EPT = (8 * NH * D + kDecThreads - 1) / kDecThreads;
         constexpr int SPL = kDecMaxSplits / 32;   // splits per lane
         const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
@@ -502,7 +629,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
-            if (lane == 0) s_lt[gg] = lt;
+            if (lane == 0) {
+                s_lt[gg] = lt;
+                if constexpr (MODE == MODE_PREFIX || MODE == MODE_SUFFIX) s_M[gg] = Mr;
+            }
         }
         __syncthreads();
         float acc[EPT];
@@ -524,8 +654,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         for (int k = 0; k < EPT; ++k) {
             const int e = tid + k * kDecThreads;
             if (e >= G * D) continue;
-            const float lt = s_lt[e / D];
-            a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc[k] / lt : 0.f);
+            if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED) {
+                const float lt = s_lt[e / D];
+                a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc[k] / lt : 0.f);
+            } else {
+                emit(b, hq0 + e / D, e % D, acc[k], s_lt[e / D], s_M[e / D], pre);
+            }
         }
         if (tid == 0) a.counters[b * Hkv + h] = 0;
         __syncthreads();
@@ -543,7 +677,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
 
     int n_done = 0;   // tiles computed by this warp
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const DecItem I = dec_item(a, s_pref, chunk, item);
+        const DecItem I = dec_item<MODE>(a, s_pref, chunk, item);
         const int hq0 = I.h * G;
         // Q^T as the MMA's B operand: n = head (8 per n-tile), k = d
         uint32_t qb[KSTEPS][NH][2];
@@ -552,14 +686,44 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             // every load is issued before any use: q words first, then (fused
             // step) the cos/sin values of this lane's pairs -- word i of a head
             // row is RoPE pair i, rotated by table row positions[b]
+            // (prefix launch: row hd of a virtual request is head hd % G of
+            // member hd / G of its chunk, G the real GQA group)
+            if constexpr (MODE != MODE_PREFIX) {
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt) {
+                        const int hd = nt * 8 + g;
+                        qb[kk][nt][0] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + t4) : 0u;
+                        qb[kk][nt][1] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + 4 + t4) : 0u;
+                    }
+            } else {
+            const uint32_t *qrow[NH];
+            bool qok[NH];
+#pragma unroll
+            for (int nt = 0; nt < NH; ++nt) {
+                const int hd = nt * 8 + g;
+                qok[nt] = hd < G;
+                qrow[nt] = q32 + hd * (D / 2);
+                {
+                    const int gr = I.b / a.cpg, c = I.b - gr * a.cpg;
+                    const int m = hd / a.G_real, j = hd - m * a.G_real;
+                    const int e = __ldg(a.grp_indptr + gr) + c * a.C + m;
+                    qok[nt] = qok[nt] && m < a.C && e < __ldg(a.grp_indptr + gr + 1);
+                    const int bm = qok[nt] ? __ldg(a.grp_reqs + e) : 0;
+                    qok[nt] = qok[nt] && bm >= 0 && bm < a.B_real;
+                    qrow[nt] = reinterpret_cast<const uint32_t *>(
+                        a.q + ((int64_t)(qok[nt] ? bm : 0) * a.Hq_real + I.h * a.G_real + j) * D);
+                }
+            }
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; ++kk)
 #pragma unroll
                 for (int nt = 0; nt < NH; ++nt) {
-                    const int hd = nt * 8 + g;
-                    qb[kk][nt][0] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + t4) : 0u;
-                    qb[kk][nt][1] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + 4 + t4) : 0u;
+                    qb[kk][nt][0] = qok[nt] ? __ldg(qrow[nt] + kk * 8 + t4) : 0u;
+                    qb[kk][nt][1] = qok[nt] ? __ldg(qrow[nt] + kk * 8 + 4 + t4) : 0u;
                 }
+            }
             if (FUSED) {
                 const int k_item = (item - (int)blockIdx.x) / (int)gridDim.x;
                 const int32_t p = k_item < kDecThreads ? s_pos[k_item] : __ldg(a.positions + I.b);
@@ -753,14 +917,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 }
             }
         }
+        const int pre_b = (MODE == MODE_SUFFIX && I.sb == 1) ? __ldcg(a.req_pre + I.b) : -1;
 #pragma unroll
         for (int k = 0; k < EPT; ++k) {
             const int e = tid + k * kDecThreads;
             if (e >= G * D) continue;
             const int gg = e / D, d = e - gg * D;
             if (I.sb == 1) {
-                a.out[((int64_t)I.b * a.Hq + hq0 + gg) * D + d] =
-                    __float2bfloat16_rn(lsum[k] > 0.f ? acc[k] / lsum[k] : 0.f);
+                if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED)
+                    a.out[((int64_t)I.b * a.Hq + hq0 + gg) * D + d] =
+                        __float2bfloat16_rn(lsum[k] > 0.f ? acc[k] / lsum[k] : 0.f);
+                else
+                    emit(I.b, hq0 + gg, d, acc[k], lsum[k], Mx[k], pre_b);
             } else {
                 const int64_t pr = ((int64_t)I.s * a.cap_batch + I.b) * a.Hq + hq0 + gg;
                 a.o_part[pr * D + d] = acc[k];
@@ -798,10 +966,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     }
 }
 
-template <int D, int S, int NH, bool FUSED>
+template <int D, int S, int NH, int MODE>
 static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
 {
-    auto kern = paged_decode_kernel<D, S, NH, FUSED>;
+    auto kern = paged_decode_kernel<D, S, NH, MODE>;
     const size_t smem = DecSmem<D, S, NH>::bytes(a.batch);
     if (smem > kSmemLimit) return PA_ERR_UNSUPPORTED;
     static size_t configured = 0;
@@ -815,12 +983,12 @@ static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
 }
 
 // Deepest ring whose shared memory fits this batch.
-template <int D, int NH, bool FUSED>
+template <int D, int NH, int MODE>
 static pa_status dispatch_decode(const DecodeArgs &a, cudaStream_t st)
 {
-    if (DecSmem<D, 4, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 4, NH, FUSED>(a, st);
-    if (DecSmem<D, 3, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 3, NH, FUSED>(a, st);
-    return launch_decode<D, 2, NH, FUSED>(a, st);
+    if (DecSmem<D, 4, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 4, NH, MODE>(a, st);
+    if (DecSmem<D, 3, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 3, NH, MODE>(a, st);
+    return launch_decode<D, 2, NH, MODE>(a, st);
 }
 static_assert(DecSmem<128, 2, 2>::bytes(kDecMaxBatch) <= kSmemLimit, "decode smem at the largest batch");
 
@@ -834,49 +1002,45 @@ struct StepInputs {
     int max_pos;
 };
 
-template <bool FUSED>
-static pa_status decode_call(const void *q, int batch, int n_q_heads, const void *k_buf, const void *v_buf,
-                             pa_kv_shape s, int layer_id, const int32_t *req_to_token, int req_rows, int max_ctx,
-                             const int32_t *req_pool_indices, const int32_t *seq_lens, float scale, void *workspace,
-                             size_t workspace_bytes, int max_splits, void *out, const StepInputs *step,
-                             cudaStream_t st)
+// Validation shared by every entry point (argument ranges, alignment).
+static pa_status check_decode(const void *q, int batch, int n_q_heads, const void *k_buf, const void *v_buf,
+                              pa_kv_shape s, int layer_id, const int32_t *req_to_token, int req_rows, int max_ctx,
+                              const int32_t *req_pool_indices, const int32_t *seq_lens, void *workspace,
+                              int max_splits, void *out)
 {
     if (batch < 0 || batch > kDecMaxBatch || n_q_heads <= 0 || s.n_layers <= 0 || s.size <= 0 ||
         s.n_kv_heads <= 0 || req_rows <= 0 || max_ctx <= 0 || max_splits < 1 || max_splits > kDecMaxSplits)
         return PA_ERR_SHAPE;
     if (layer_id < 0 || layer_id >= s.n_layers) return PA_ERR_SHAPE;
     if (n_q_heads % s.n_kv_heads != 0) return PA_ERR_SHAPE;
-    if (step && step->max_pos <= 0) return PA_ERR_SHAPE;
     const int G = n_q_heads / s.n_kv_heads;
     if (G > 16 || (s.head_dim != 64 && s.head_dim != 128)) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)s.n_layers * s.size >= (int64_t)INT32_MAX - 16) return PA_ERR_SHAPE;
     if (!workspace) return PA_ERR_NULL;
     if (!aligned256(workspace)) return PA_ERR_ALIGN;
-    const DecodeWsLayout ws = decode_ws_layout(workspace_bytes, n_q_heads, s.n_kv_heads, s.head_dim, max_splits);
-    if (ws.cap_batch < batch || ws.total > workspace_bytes) return PA_ERR_WORKSPACE;
     if (batch == 0) return PA_OK;
     if (!q || !k_buf || !v_buf || !req_to_token || !req_pool_indices || !seq_lens || !out) return PA_ERR_NULL;
     if (!aligned16(q) || !aligned16(k_buf) || !aligned16(v_buf) || !aligned16(out) || !aligned4(req_to_token) ||
         !aligned4(req_pool_indices) || !aligned4(seq_lens))
         return PA_ERR_ALIGN;
-    if (step) {
-        if (!step->k_new || !step->v_new || !step->positions || !step->loc || !step->cos_tab || !step->sin_tab)
-            return PA_ERR_NULL;
-        if (!aligned16(step->k_new) || !aligned16(step->v_new) || !aligned4(step->positions) ||
-            !aligned4(step->loc) || !aligned16(step->cos_tab) || !aligned16(step->sin_tab))
-            return PA_ERR_ALIGN;
-    }
+    return PA_OK;
+}
 
-    if ((int64_t)s.n_layers * s.size >= (int64_t)INT32_MAX - 16) return PA_ERR_SHAPE;
-    DecodeArgs a;
+// Launch arguments for `batch` requests of `n_q_heads` heads whose split
+// partials live in the decode layout `ws` at `wbase`; errors go to `err`.
+static bool fill_decode_args(DecodeArgs &a, const void *q, int batch, int n_q_heads, const void *k_buf,
+                             const void *v_buf, pa_kv_shape s, int layer_id, const int32_t *req_to_token,
+                             int req_rows, int max_ctx, const int32_t *req_pool_indices, const int32_t *seq_lens,
+                             float scale, int max_splits, void *out, int32_t *err, const DecodeWsLayout &ws,
+                             unsigned char *wbase)
+{
     memset(&a, 0, sizeof a);
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)s.n_kv_heads * s.head_dim, (cuuint64_t)s.n_layers * s.size};
-        const cuuint64_t strides[1] = {(cuuint64_t)s.n_kv_heads * s.head_dim * 2};
-        const cuuint32_t box[2] = {64, kDecTile};
-        if (!encode_tmap_bf16(&a.tm_k, k_buf, 2, dims, strides, box) ||
-            !encode_tmap_bf16(&a.tm_v, v_buf, 2, dims, strides, box))
-            return PA_ERR_CUDA;
-    }
+    const cuuint64_t dims[2] = {(cuuint64_t)s.n_kv_heads * s.head_dim, (cuuint64_t)s.n_layers * s.size};
+    const cuuint64_t strides[1] = {(cuuint64_t)s.n_kv_heads * s.head_dim * 2};
+    const cuuint32_t box[2] = {64, kDecTile};
+    if (!encode_tmap_bf16(&a.tm_k, k_buf, 2, dims, strides, box) ||
+        !encode_tmap_bf16(&a.tm_v, v_buf, 2, dims, strides, box))
+        return false;
     a.layer_row0 = layer_id * s.size;
     const int64_t layer_off = (int64_t)layer_id * s.size * s.n_kv_heads * s.head_dim;
     a.q = static_cast<const __nv_bfloat16 *>(q);
@@ -886,15 +1050,14 @@ static pa_status decode_call(const void *q, int batch, int n_q_heads, const void
     a.req_pool_indices = req_pool_indices;
     a.seq_lens = seq_lens;
     a.out = static_cast<__nv_bfloat16 *>(out);
-    unsigned char *w = static_cast<unsigned char *>(workspace);
-    a.err = reinterpret_cast<int32_t *>(w);
-    a.counters = reinterpret_cast<int32_t *>(w + ws.counters_off);
-    a.ml_part = reinterpret_cast<float *>(w + ws.ml_off);
-    a.o_part = reinterpret_cast<float *>(w + ws.o_off);
+    a.err = err;
+    a.counters = reinterpret_cast<int32_t *>(wbase + ws.counters_off);
+    a.ml_part = reinterpret_cast<float *>(wbase + ws.ml_off);
+    a.o_part = reinterpret_cast<float *>(wbase + ws.o_off);
     a.batch = batch;
     a.Hq = n_q_heads;
     a.Hkv = s.n_kv_heads;
-    a.G = G;
+    a.G = n_q_heads / s.n_kv_heads;
     a.size = s.size;
     a.req_rows = req_rows;
     a.max_ctx = max_ctx;
@@ -902,7 +1065,44 @@ static pa_status decode_call(const void *q, int batch, int n_q_heads, const void
     a.max_splits = max_splits;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     a.early_meta = launch_overlap() == PA_OVERLAP_EARLY_METADATA;
+    return true;
+}
+
+template <int MODE>
+static pa_status dispatch_mode(const DecodeArgs &a, int head_dim, cudaStream_t st)
+{
+    if (head_dim == 128) return a.G > 8 ? dispatch_decode<128, 2, MODE>(a, st) : dispatch_decode<128, 1, MODE>(a, st);
+    return a.G > 8 ? dispatch_decode<64, 2, MODE>(a, st) : dispatch_decode<64, 1, MODE>(a, st);
+}
+
+template <int MODE>
+static pa_status decode_call(const void *q, int batch, int n_q_heads, const void *k_buf, const void *v_buf,
+                             pa_kv_shape s, int layer_id, const int32_t *req_to_token, int req_rows, int max_ctx,
+                             const int32_t *req_pool_indices, const int32_t *seq_lens, float scale, void *workspace,
+                             size_t workspace_bytes, int max_splits, void *out, const StepInputs *step,
+                             cudaStream_t st)
+{
+    pa_status rc = check_decode(q, batch, n_q_heads, k_buf, v_buf, s, layer_id, req_to_token, req_rows, max_ctx,
+                                req_pool_indices, seq_lens, workspace, max_splits, out);
+    if (rc != PA_OK) return rc;
+    if (step && step->max_pos <= 0) return PA_ERR_SHAPE;
+    const DecodeWsLayout ws = decode_ws_layout(workspace_bytes, n_q_heads, s.n_kv_heads, s.head_dim, max_splits);
+    if (ws.cap_batch < batch || ws.total > workspace_bytes) return PA_ERR_WORKSPACE;
+    if (batch == 0) return PA_OK;
     if (step) {
+        if (!step->k_new || !step->v_new || !step->positions || !step->loc || !step->cos_tab || !step->sin_tab)
+            return PA_ERR_NULL;
+        if (!aligned16(step->k_new) || !aligned16(step->v_new) || !aligned4(step->positions) ||
+            !aligned4(step->loc) || !aligned16(step->cos_tab) || !aligned16(step->sin_tab))
+            return PA_ERR_ALIGN;
+    }
+    unsigned char *w = static_cast<unsigned char *>(workspace);
+    DecodeArgs a;
+    if (!fill_decode_args(a, q, batch, n_q_heads, k_buf, v_buf, s, layer_id, req_to_token, req_rows, max_ctx,
+                          req_pool_indices, seq_lens, scale, max_splits, out, reinterpret_cast<int32_t *>(w), ws, w))
+        return PA_ERR_CUDA;
+    if (step) {
+        const int64_t layer_off = (int64_t)layer_id * s.size * s.n_kv_heads * s.head_dim;
         a.k_new = static_cast<const __nv_bfloat16 *>(step->k_new);
         a.v_new = static_cast<const __nv_bfloat16 *>(step->v_new);
         a.positions = step->positions;
@@ -913,8 +1113,7 @@ static pa_status decode_call(const void *q, int batch, int n_q_heads, const void
         a.k_layer_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(k_buf)) + layer_off;
         a.v_layer_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(v_buf)) + layer_off;
     }
-    if (s.head_dim == 128) return G > 8 ? dispatch_decode<128, 2, FUSED>(a, st) : dispatch_decode<128, 1, FUSED>(a, st);
-    return G > 8 ? dispatch_decode<64, 2, FUSED>(a, st) : dispatch_decode<64, 1, FUSED>(a, st);
+    return dispatch_mode<MODE>(a, s.head_dim, st);
 }
 
 }  // namespace pa

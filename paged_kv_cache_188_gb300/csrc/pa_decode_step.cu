@@ -14,7 +14,7 @@ extern "C" pa_status pa_decode_step(const void *q, const void *k_new, const void
                                     cudaStream_t st)
 {
     const StepInputs step{k_new, v_new, positions, loc, cos_tab, sin_tab, max_pos};
-    return decode_call<true>(q, batch, n_q_heads, k_buf, v_buf, s, layer_id, req_to_token, req_rows, max_ctx,
+    return decode_call<MODE_FUSED>(q, batch, n_q_heads, k_buf, v_buf, s, layer_id, req_to_token, req_rows, max_ctx,
                        req_pool_indices, seq_lens, scale, workspace, workspace_bytes, max_splits, out, &step, st);
 }
 

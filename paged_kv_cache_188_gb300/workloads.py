@@ -266,6 +266,24 @@ def cfg_lens_lognormal(n, median, sigma, cap, seed):
     return [int(min(cap, max(1, round(math.exp(math.log(median) + sigma * float(v)))))) for v in z]
 
 
+def prefix_groups(lens, group_size, prefix_len, page_size):
+    """Group arrays of a batch built with ``shared_prefix=(group_size, prefix_len)``:
+    members of group g are requests g*group_size .. ; the common prefix is the
+    shortest shared part of its members (the page holding a request's newest
+    token is private).  Returns int32 tensors (indptr, reqs, prefix)."""
+    B = len(lens)
+    n_groups = -(-B // group_size)
+    indptr = [min(g * group_size, B) for g in range(n_groups + 1)]
+    reqs = list(range(B))
+    prefix = []
+    for g in range(n_groups):
+        members = range(indptr[g], indptr[g + 1])
+        prefix.append(min(min(max(int(lens[b]) - 1, 0) // page_size, prefix_len // page_size) * page_size
+                          for b in members))
+    return (torch.tensor(indptr, dtype=torch.int32), torch.tensor(reqs, dtype=torch.int32),
+            torch.tensor(prefix, dtype=torch.int32))
+
+
 def config1(device="cpu"):
     """Single-layer paged decode, B=1, Hq=8, Hkv=2, D=64, seq 256, 16 pages."""
     return make_decode_step(lens=[256], n_q_heads=8, n_kv_heads=2, head_dim=64, n_layers=1,

@@ -152,3 +152,23 @@ def test_prefill_variants_host_validation(lib):
     assert dense(hq=6, hkv=4) == 2
     assert dense(ws=0) == 1
     assert dense(last=FAKE + 8) == 3
+
+
+def test_cascade_workspace_and_validation(lib):
+    caps = (32, 4, 8, 64)
+    small = api.pa_cascade_workspace_bytes(*caps, 32, 8, 128)
+    assert small >= api.pa_decode_workspace_bytes(32, 32, 8, 128, 64)
+    assert api.pa_cascade_workspace_bytes(64, 8, 8, 64, 32, 8, 128) > small
+    assert api.pa_cascade_workspace_bytes(32, 4, 0, 64, 32, 8, 128) == 0        # max_group_size >= 1
+    assert api.pa_cascade_workspace_bytes(32, 4096, 64, 64, 32, 8, 128) == 0    # virtual batch over 4096
+    P = ctypes.c_void_p
+    c = api.CascadeCaps(*caps)
+    call = lambda **kw: lib.pa_paged_decode_attn_cascade(
+        P(FAKE), kw.get("b", 1), 32, P(FAKE), P(FAKE), api.KvShape(1, 64, 8, 128), 0, P(FAKE), 1, 16, P(FAKE),
+        P(FAKE), P(kw.get("ip", FAKE)), P(FAKE), P(FAKE), kw.get("ng", 1), c, 0.1, P(FAKE), kw.get("wsb", small),
+        P(FAKE), None)
+    assert call(b=33) == 2                        # batch over caps.max_batch
+    assert call(ng=5) == 2                        # groups over caps.max_groups
+    assert call(wsb=small - 1) == 5
+    assert call(ip=0) == 1
+    assert call(ip=FAKE + 2) == 3
