@@ -171,9 +171,10 @@ struct DecSmem {
     static constexpr int kStage = 2 * kTile;
     static constexpr int kRing = S * kStage;                             // per warp
     static constexpr int kScratchOff = kDecWarps * kRing;
-    // half the warps' O states [4][G][D] fp32 at a time, later the split merge
+    // half the warps' O states [4][G][D + 4] fp32 at a time, later the split merge
     // [sb][G][2] + [sb][G] + [G]
-    static constexpr int kCombine = (kDecWarps / 2) * 8 * NH * D * 4;
+    static constexpr int kCombineStride = D + 4;   // padded row: the four t4 lanes of a store hit distinct banks
+    static constexpr int kCombine = (kDecWarps / 2) * 8 * NH * kCombineStride * 4;
     static constexpr int kMerge = (3 * kDecMaxSplits * 8 * NH + 16 * NH) * 4;
     static constexpr int kScratch = kCombine > kMerge ? kCombine : kMerge;
     static constexpr int kMaskOff = kScratchOff + kScratch;
@@ -890,7 +891,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                         for (int e = 0; e < 4; ++e) {
                             const int hd = nt * 8 + 2 * t4 + (e & 1);
                             const int d = dm * 16 + g + 8 * (e >> 1);
-                            if (hd < G) scratch[(wl * G + hd) * D + d] = o[dm][nt][e];
+                            if (hd < G) scratch[(wl * G + hd) * L::kCombineStride + d] = o[dm][nt][e];
                         }
             }
             __syncthreads();
@@ -913,7 +914,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                     const int wg = rr * (kDecWarps / 2) + w;
                     const float wt = ex2(s_m[wg][gg] - Mr);
                     lsum[k] += wt * s_l[wg][gg];
-                    acc[k] += wt * scratch[(w * G + gg) * D + d];
+                    acc[k] += wt * scratch[(w * G + gg) * L::kCombineStride + d];
                 }
             }
         }
