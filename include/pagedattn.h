@@ -183,9 +183,10 @@ pa_status pa_rope_packed(void *q, int n_q_heads, void *k, int n_kv_heads, int he
  * a fixed order (run-to-run bit-identical).
  * Supported: head_dim in {64, 128}; 1 <= G <= 16; 1 <= max_splits <= 128;
  * batch <= 4096 and <= the workspace's cap_batch for these head counts and
- * max_splits.  K/V rows are moved by bulk-async (TMA) row copies: k_buf and
- * v_buf must be 16-byte aligned, which with head_dim 64/128 makes every row
- * 16-byte aligned. */
+ * max_splits.  A 16-token tile whose positions sit on one page moves as TMA
+ * boxes, any other tile as 16-byte cp.async rows: k_buf and v_buf must be
+ * 16-byte aligned, which with head_dim 64/128 makes every row 16-byte
+ * aligned. */
 pa_status pa_paged_decode_attn(const void *q, int batch, int n_q_heads, const void *k_buf,
                                const void *v_buf, pa_kv_shape s, int layer_id,
                                const int32_t *req_to_token, int req_rows, int max_ctx,
