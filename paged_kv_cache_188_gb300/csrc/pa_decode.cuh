@@ -41,8 +41,9 @@
 //    head) -- an integer atomic ticket, no waiting -- merges all splits in
 //    split order (deterministic), writes bf16 and re-arms the ticket to zero.
 //    The ticket is an acquire-release atomic, so the merging CTA needs no
-//    separate fence; the first eight splits' partials travel with the (m, l)
-//    pairs, the weights are warp-parallel, further splits eight at a time.
+//    separate fence; the first 20 splits' partials (8 when G > 8) travel with
+//    the (m, l) pairs, the weights are warp-parallel, further splits follow
+//    in batches of the same size.
 //  * Fused decode step (FUSED = true, pa_decode_step): q is rotated (RoPE)
 //    in registers as it is loaded, and the CTA holding the last split of a
 //    (request, kv head) writes that head's new K (rotated) and V rows at
@@ -550,8 +551,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     // ------------------------------------------------------ split merge
     // The CTA whose ticket completes (b, h) merges all its splits in split
     // order, writes bf16 and re-arms the ticket.  Whole-CTA; uses the scratch.
-    // The first eight splits of this thread's output elements are requested
-    // before the (m, l) pairs, so both travel in one round trip; the split
+    // The first 20 splits (8 when G > 8) of this thread's output elements are
+    // requested before the (m, l) pairs, so both travel in one round trip; the split
     // weights are computed warp-parallel (a warp per q head, lanes over
     // splits, shuffle max and sum).
     int pend_prev = -1;                        // thread 0: pending ticket result
@@ -592,17 +593,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         constexpr int SPL = kDecMaxSplits / 32;   // splits per lane
         const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
         const float *obase = a.o_part + ((int64_t)b * a.Hq + hq0) * D;
-        float v[EPT][8];
-        auto load8 = [&](int ss) {
+        // splits per element per round trip: 20 covers the one-wave plans'
+        // 19 splits per head in one trip (registers EPT * SB)
+        constexpr int SB = EPT <= 4 ? 20 : 8;
+        float v[EPT][SB];
+        auto load_batch = [&](int ss) {
 #pragma unroll
             for (int k = 0; k < EPT; ++k) {
                 const int e = tid + k * kDecThreads;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < SB; ++j)
                     v[k][j] = (e < G * D && ss + j < sb) ? __ldcg(obase + e + (ss + j) * split_stride) : 0.f;
             }
         };
-        load8(0);
+        load_batch(0);
         const int64_t ml_stride = (int64_t)a.cap_batch * a.Hq * 2;   // floats per split
         for (int gg = warp; gg < G; gg += kDecWarps) {
             const float *ml = a.ml_part + ((int64_t)b * a.Hq + hq0 + gg) * 2;
@@ -639,15 +643,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         float acc[EPT];
 #pragma unroll
         for (int k = 0; k < EPT; ++k) acc[k] = 0.f;
-        for (int ss = 0; ss < sb; ss += 8) {   // each element summed in split order
-            if (ss > 0) load8(ss);
+        for (int ss = 0; ss < sb; ss += SB) {   // each element summed in split order
+            if (ss > 0) load_batch(ss);
 #pragma unroll
             for (int k = 0; k < EPT; ++k) {
                 const int e = tid + k * kDecThreads;
                 if (e >= G * D) continue;
                 const int gg = e / D;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < SB; ++j)
                     if (ss + j < sb) acc[k] += s_w[(ss + j) * G + gg] * v[k][j];
             }
         }
