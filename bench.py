@@ -56,8 +56,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, valid only while the kernel source is unchanged (sha256 prefix).
-NCU_TRAFFIC = {"decode": {"sha": "724e877bd47c2399", "ratio": round((537.544448 + 3.359232) / 537.460768, 5),
-                          "capture": "ncu, 4 x 32K tokens, one layer: dram read+write 540.90 MB for "
+NCU_TRAFFIC = {"decode": {"sha": "5d3acc4d2afe6e0a", "ratio": round((537.539584 + 2.984192) / 537.460768, 5),
+                          "capture": "ncu, 4 x 32K tokens, one layer: dram read+write 540.52 MB for "
                                      "537.46 MB algorithmic; scaled to this workload by algorithmic bytes"}}
 
 
