@@ -255,11 +255,14 @@ class DecodeSweep:
         self.seq = [torch.tensor([n], dtype=torch.int32, device=dev) for n in SWEEP]
         self.pos = [torch.tensor([n - 1], dtype=torch.int32, device=dev) for n in SWEEP]
         self.loc = [kv.req_to_token[row, n - 1:n].clone() for n in SWEEP]
-        self.ws = api.alloc_workspace(api.pa_decode_workspace_bytes(1, HQ, HKV, D, MAX_SPLITS), dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.scale = 1.0 / math.sqrt(D)
-        self.stream = torch.cuda.Stream(dev)
-        self.stream.wait_stream(torch.cuda.current_stream(dev))
+        self.ws = self.stream = None
+        if dev.type == "cuda":
+            # the reference arm builds the same inputs on the host and needs neither
+            self.ws = api.alloc_workspace(api.pa_decode_workspace_bytes(1, HQ, HKV, D, MAX_SPLITS), dev)
+            self.stream = torch.cuda.Stream(dev)
+            self.stream.wait_stream(torch.cuda.current_stream(dev))
 
     def layer_call(self, p, l, what=("rope", "store", "decode")):
         a, kv, s = self.api, self.kv, self.stream
