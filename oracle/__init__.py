@@ -10,7 +10,8 @@ compiled with gcc into ``liboracle.so`` next to this file.  This module only
 marshals numpy arrays through ctypes.  Every function states the definition it
 computes and the page passage it follows in ``oracle.c``.
 
-bf16 tensors are passed as ``numpy.uint16`` arrays of bit patterns.
+bf16 tensors are passed as ``numpy.uint16`` arrays of bit patterns, fp8
+(e4m3) cache bytes as ``numpy.uint8``.
 """
 from __future__ import annotations
 
@@ -62,6 +63,17 @@ def _load():
         lib.ora_prefill.argtypes = [P, i64, i32, P, P, i32, i64, i32, i32, i32,
                                     P, P, i32, P, i32, i32, P, dbl, P, P, i64, P]
         lib.ora_prefill.restype = i32
+        lib.ora_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.ora_e4m3_to_f64.restype = dbl
+        lib.ora_f32_to_e4m3.argtypes = [ctypes.c_float]
+        lib.ora_f32_to_e4m3.restype = ctypes.c_uint8
+        lib.ora_f32_to_e4m3_array.argtypes = [P, i64, P]
+        lib.ora_f32_to_e4m3_array.restype = None
+        lib.ora_kv_store_fp8.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, P, i64, P, P]
+        lib.ora_kv_store_fp8.restype = i32
+        lib.ora_decode_fp8.argtypes = [P, i32, i32, P, P, i32, i64, i32, i32, i32,
+                                       P, i32, i32, P, P, dbl, P, P, P, P, i64, P]
+        lib.ora_decode_fp8.restype = i32
         _lib = lib
     return _lib
 
@@ -188,4 +200,71 @@ def prefill(q_bits, k_buf_bits, v_buf_bits, layer, qo_indptr, kv_indptr, req_to_
                              rp, r2t.shape[0], r2t.shape[1], rpip, float(scale),
                              st, sh, nsel, out.ctypes.data_as(ctypes.c_void_p))
     _check(rc, "prefill")
+    return out
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Exact values of e4m3 bytes (elementwise; NaN for 0x7F / 0xFF)."""
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    return np.array([lib.ora_e4m3_to_f64(int(b)) for b in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def f32_to_e4m3(x) -> np.ndarray:
+    """Nearest e4m3 bytes to float32 values, ties to even, finite overflow
+    saturating to +-448.  See ``ora_f32_to_e4m3``."""
+    x, xp = _c(x, np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().ora_f32_to_e4m3_array(xp, x.size, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def kv_store_fp8(k_buf, v_buf, layer, k_new_bits, v_new_bits, loc, k_scale, v_scale):
+    """Return copies of the two [n_layers, size, Hkv, D] byte buffers with the
+    new tokens' rows quantised to e4m3 by the per-(layer, kv head) scales
+    [n_layers, Hkv] and written at ``loc``.  See ``ora_kv_store_fp8``."""
+    kb = np.array(k_buf, dtype=np.uint8, copy=True, order="C")
+    vb = np.array(v_buf, dtype=np.uint8, copy=True, order="C")
+    n_layers, size, Hkv, D = kb.shape
+    kn, knp = _c(k_new_bits, np.uint16)
+    vn, vnp = _c(v_new_bits, np.uint16)
+    lc, lp = _c(loc, np.int32)
+    ks, ksp = _c(k_scale, np.float32)
+    vs, vsp = _c(v_scale, np.float32)
+    assert ks.shape == (n_layers, Hkv) and vs.shape == (n_layers, Hkv)
+    rc = _load().ora_kv_store_fp8(kb.ctypes.data_as(ctypes.c_void_p), vb.ctypes.data_as(ctypes.c_void_p),
+                                  n_layers, size, Hkv, D, layer, knp, vnp, lp, lc.size, ksp, vsp)
+    _check(rc, "kv_store_fp8")
+    return kb, vb
+
+
+def decode_fp8(q_bits, k_buf, v_buf, layer, req_to_token, req_pool_indices, seq_lens, scale,
+               k_scale, v_scale, sel=None):
+    """Packed decode attention in float64 over an e4m3 cache with per-(layer,
+    kv head) scales.  Same shapes and ``sel`` as ``decode``."""
+    q, qp = _c(q_bits, np.uint16)
+    B, Hq, D = q.shape
+    kb, kp = _c(k_buf, np.uint8)
+    vb, vp = _c(v_buf, np.uint8)
+    n_layers, size, Hkv, D2 = kb.shape
+    assert D2 == D and vb.shape == kb.shape
+    ks, ksp = _c(k_scale, np.float32)
+    vs, vsp = _c(v_scale, np.float32)
+    assert ks.shape == (n_layers, Hkv) and vs.shape == (n_layers, Hkv)
+    r2t, rp = _c(req_to_token, np.int32)
+    rpi, rpip = _c(req_pool_indices, np.int32)
+    sl, slp = _c(seq_lens, np.int32)
+    if sel is None:
+        out = np.empty((B, Hq, D), dtype=np.float64)
+        sb = sh = None
+        nsel = 0
+    else:
+        sbb, sb = _c(sel[0], np.int32)
+        shh, sh = _c(sel[1], np.int32)
+        nsel = sbb.size
+        out = np.empty((nsel, D), dtype=np.float64)
+    rc = _load().ora_decode_fp8(qp, B, Hq, kp, vp, n_layers, size, Hkv, D, layer,
+                                rp, r2t.shape[0], r2t.shape[1], rpip, slp, float(scale), ksp, vsp,
+                                sb, sh, nsel, out.ctypes.data_as(ctypes.c_void_p))
+    _check(rc, "decode_fp8")
     return out

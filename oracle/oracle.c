@@ -330,3 +330,171 @@ int ora_prefill(const uint16_t *q, int64_t T, int Hq, const uint16_t *k_buf,
     free(scores);
     return ORA_OK;
 }
+
+/* ------------------------------------------------------ fp8 (e4m3) cache */
+
+/* fp8 e4m3 KV cache with per-head scales.  The only mention on the pages is
+ * page "e58a728 / docs/developer/architecture.md", whose change list names an
+ * fp8 test among the CUDA kernel sources; everything below is a reading.
+ * Format: the OCP 8-bit float E4M3 -- 1 sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits, no infinities, S.1111.111 is NaN, largest finite 448.
+ * Reading (the pages give no scheme): one fp32 scale per (layer, kv head) for
+ * K and one for V, supplied by the caller; stored byte =
+ * e4m3(fp32(x) / scale) with the division in fp32 (IEEE, nearest) and the
+ * conversion rounding to nearest, ties to even, finite values beyond 448
+ * saturating to +-448; the value read back is e4m3_value(byte) * scale. */
+
+/* Exact value of an e4m3 byte (NaN for the two NaN codes). */
+double ora_e4m3_to_f64(uint8_t b)
+{
+    int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = e == 0 ? ldexp((double)m, -9)             /* subnormal: m/8 * 2^-6 */
+                      : ldexp(8.0 + m, e - 10);          /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Nearest e4m3 byte to a float, ties to even, saturating finite overflow
+ * (and infinities) to +-448; NaN -> 0x7F. */
+uint8_t ora_f32_to_e4m3(float xf)
+{
+    double x = (double)xf;
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);             /* a = f * 2^e, f in [0.5, 1): a in [2^(e-1), 2^e) */
+    int qexp = e - 4;         /* spacing of 4-significant-bit numbers near a */
+    if (qexp < -9)
+        qexp = -9;            /* subnormal range: fixed spacing 2^-9 */
+    double r = nearbyint(ldexp(a, -qexp)); /* exact scaling, then nearest-even */
+    double v = ldexp(r, qexp);             /* <= 448 since a < 448 */
+    if (v == 0.0)
+        return sign;
+    int ev;
+    frexp(v, &ev);
+    int E = ev - 1 + 7;       /* biased exponent of v = 2^(ev-1) * (1 + m/8) */
+    if (E <= 0)               /* subnormal: v = m * 2^-9 */
+        return (uint8_t)(sign | (uint8_t)ldexp(v, 9));
+    int m = (int)(ldexp(v, -(ev - 1)) * 8.0) - 8;
+    return (uint8_t)(sign | (E << 3) | m);
+}
+
+void ora_f32_to_e4m3_array(const float *x, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = ora_f32_to_e4m3(x[i]);
+}
+
+/* Quantising KV store: k8_buf[layer, loc[t], h, :] = e4m3(k_new[t, h, :] /
+ * k_scale[layer, h]), the same for V; buffers [n_layers, size, Hkv, D] bytes,
+ * scales [n_layers, Hkv] fp32.  Locations are checked before anything is
+ * written. */
+int ora_kv_store_fp8(uint8_t *k_buf, uint8_t *v_buf, int n_layers, int64_t size,
+                     int Hkv, int D, int layer, const uint16_t *k_new,
+                     const uint16_t *v_new, const int32_t *loc, int64_t T,
+                     const float *k_scale, const float *v_scale)
+{
+    if (layer < 0 || layer >= n_layers || Hkv <= 0 || D <= 0 || T < 0)
+        return ORA_ERR_SHAPE;
+    for (int64_t t = 0; t < T; ++t)
+        if (loc[t] < 0 || (int64_t)loc[t] >= size)
+            return ORA_ERR_INDEX;
+    const int64_t row = (int64_t)Hkv * D;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t dst = ((int64_t)layer * size + loc[t]) * row;
+        for (int h = 0; h < Hkv; ++h) {
+            float ks = k_scale[(int64_t)layer * Hkv + h], vs = v_scale[(int64_t)layer * Hkv + h];
+            for (int d = 0; d < D; ++d) {
+                int64_t j = (int64_t)h * D + d;
+                float kx = (float)ora_bf16_to_f64(k_new[t * row + j]);
+                float vx = (float)ora_bf16_to_f64(v_new[t * row + j]);
+                k_buf[dst + j] = ora_f32_to_e4m3(kx / ks);
+                v_buf[dst + j] = ora_f32_to_e4m3(vx / vs);
+            }
+        }
+    }
+    return ORA_OK;
+}
+
+/* Packed decode attention over an fp8 cache: as ora_decode, with key j of kv
+ * head h read as e4m3_value(K8[slot_j, h, :]) * k_scale[layer, h] and value
+ * rows likewise with v_scale.  Same output, selection and checks. */
+int ora_decode_fp8(const uint16_t *q, int B, int Hq, const uint8_t *k_buf,
+                   const uint8_t *v_buf, int n_layers, int64_t size, int Hkv,
+                   int D, int layer, const int32_t *req_to_token, int req_rows,
+                   int max_ctx, const int32_t *req_pool_indices,
+                   const int32_t *seq_lens, double scale, const float *k_scale,
+                   const float *v_scale, const int32_t *sel_b,
+                   const int32_t *sel_h, int64_t n_sel, double *out)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || layer < 0 || layer >= n_layers || D <= 0)
+        return ORA_ERR_SHAPE;
+    const int G = Hq / Hkv;
+    const int64_t npairs = sel_b ? n_sel : (int64_t)B * Hq;
+    for (int64_t i = 0; i < npairs; ++i) {
+        int b = sel_b ? sel_b[i] : (int)(i / Hq);
+        int hq = sel_b ? sel_h[i] : (int)(i % Hq);
+        if (b < 0 || b >= B || hq < 0 || hq >= Hq)
+            return ORA_ERR_SHAPE;
+        int row = req_pool_indices[b];
+        int n = seq_lens[b];
+        if (row < 0 || row >= req_rows || n < 0 || n > max_ctx)
+            return ORA_ERR_INDEX;
+        for (int j = 0; j < n; ++j) {
+            int32_t s = req_to_token[(int64_t)row * max_ctx + j];
+            if (s < 0 || (int64_t)s >= size)
+                return ORA_ERR_INDEX;
+        }
+    }
+    double *scores = (double *)malloc(sizeof(double) * (size_t)(max_ctx > 0 ? max_ctx : 1));
+    if (!scores)
+        return ORA_ERR_NOMEM;
+    const int64_t slot_stride = (int64_t)Hkv * D;
+    for (int64_t i = 0; i < npairs; ++i) {
+        int b = sel_b ? sel_b[i] : (int)(i / Hq);
+        int hq = sel_b ? sel_h[i] : (int)(i % Hq);
+        int h = hq / G;
+        int n = seq_lens[b];
+        const int32_t *slots = req_to_token + (int64_t)req_pool_indices[b] * max_ctx;
+        const uint16_t *qv = q + ((int64_t)b * Hq + hq) * D;
+        const uint8_t *k0 = k_buf + (int64_t)layer * size * slot_stride + (int64_t)h * D;
+        const uint8_t *v0 = v_buf + (int64_t)layer * size * slot_stride + (int64_t)h * D;
+        const double ks = (double)k_scale[(int64_t)layer * Hkv + h];
+        const double vs = (double)v_scale[(int64_t)layer * Hkv + h];
+        double *o = out + i * D;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        if (n <= 0)
+            continue;
+        double m = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+            const uint8_t *kr = k0 + (int64_t)slots[j] * slot_stride;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += ora_bf16_to_f64(qv[d]) * (ora_e4m3_to_f64(kr[d]) * ks);
+            scores[j] = scale * dot;
+            if (scores[j] > m)
+                m = scores[j];
+        }
+        double denom = 0.0;
+        for (int j = 0; j < n; ++j) {
+            scores[j] = exp(scores[j] - m);
+            denom += scores[j];
+        }
+        for (int j = 0; j < n; ++j) {
+            const uint8_t *vr = v0 + (int64_t)slots[j] * slot_stride;
+            double w = scores[j] / denom;
+            for (int d = 0; d < D; ++d)
+                o[d] += w * (ora_e4m3_to_f64(vr[d]) * vs);
+        }
+    }
+    free(scores);
+    return ORA_OK;
+}

@@ -382,3 +382,116 @@ def test_prefill_packing_is_per_request():
     sel = oracle.prefill(bits(pb.q), kb, vb, 0, pb.qo_indptr.numpy(), pb.kv_indptr.numpy(), r2t, rpi,
                          pb.scale, sel=(np.array([9, 0], np.int32), np.array([1, 0], np.int32)))
     np.testing.assert_array_equal(sel, out[[9, 0], [1, 0]])
+
+
+# ------------------------------------------------------- fp8 (e4m3) cache
+
+def _torch_e4m3(x: np.ndarray) -> np.ndarray:
+    """torch's float32 -> float8_e4m3fn conversion (nearest, ties to even;
+    NaN above 464, where rounding reaches 480 and the oracle saturates)."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _torch_e4m3_values(codes: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+
+
+def test_e4m3_values_match_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_to_f64(codes)
+    ref = _torch_e4m3_values(codes)
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    np.testing.assert_array_equal(ours[fin], ref[fin])
+    assert np.isnan(ours[[0x7F, 0xFF]]).all() and ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+    assert np.signbit(ours[0x80]) and ours[0x80] == 0.0
+
+
+def test_e4m3_encoding_matches_torch_up_to_464():
+    g = np.random.default_rng(11)
+    parts = [g.standard_normal(4000) * 2.0 ** k for k in range(-12, 9)]
+    finite = _torch_e4m3_values(np.arange(256, dtype=np.uint8))
+    finite = np.unique(finite[~np.isnan(finite)])
+    mids = (finite[1:] + finite[:-1]) / 2          # every tie between neighbouring codes
+    parts += [finite, mids, -mids, np.array([0.0, -0.0, 447.9, 463.9, 464.0, -464.0])]
+    x = np.concatenate(parts).astype(np.float32)
+    x = x[np.abs(x) <= 464]
+    np.testing.assert_array_equal(oracle.f32_to_e4m3(x), _torch_e4m3(x))
+
+
+def test_e4m3_saturates_and_round_trips():
+    big = np.array([448.0, 464.5, 479.9, 480.0, 1000.0, 3.0e38, np.inf], np.float32)
+    np.testing.assert_array_equal(oracle.f32_to_e4m3(big), np.full(7, 0x7E, np.uint8))
+    np.testing.assert_array_equal(oracle.f32_to_e4m3(-big), np.full(7, 0xFE, np.uint8))
+    assert oracle.f32_to_e4m3(np.array([np.nan], np.float32))[0] & 0x7F == 0x7F
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    vals = oracle.e4m3_to_f64(codes).astype(np.float32)
+    np.testing.assert_array_equal(oracle.f32_to_e4m3(vals), codes)
+
+
+def test_kv_store_fp8_matches_torch_quantisation():
+    g = W.generator(23)
+    L, size, Hkv, D = 2, 48, 3, 16
+    kb = np.full((L, size, Hkv, D), 0x7F, np.uint8)
+    vb = np.full((L, size, Hkv, D), 0x7F, np.uint8)
+    kn = W.bf16_normal((9, Hkv, D), g) * 40
+    vn = W.bf16_normal((9, Hkv, D), g)
+    kn[0, 0, :4] = torch.tensor([1e4, -1e4, 0.0, -0.0])   # saturating and signed-zero entries
+    ks = np.array([[0.5, 0.03, 1.7], [0.25, 0.11, 3.0]], np.float32)
+    vs = np.array([[0.01, 0.2, 0.007], [0.004, 0.09, 1.0]], np.float32)
+    loc = torch.randperm(size, generator=g)[:9].numpy().astype(np.int32)
+    k2, v2 = oracle.kv_store_fp8(kb, vb, 1, bits(kn), bits(vn), loc, ks, vs)
+    kw, vw = kb.copy(), vb.copy()
+    for new, sc, want in ((kn, ks, kw), (vn, vs, vw)):
+        q = (new.float() / torch.from_numpy(sc[1])[None, :, None]).clamp(-448, 448)   # fp32 division
+        want[1, loc] = q.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(k2, kw)
+    np.testing.assert_array_equal(v2, vw)
+    with pytest.raises(oracle.OracleError):
+        oracle.kv_store_fp8(kb, vb, 1, bits(kn), bits(vn), np.r_[loc[:8], size].astype(np.int32), ks, vs)
+
+
+def _fp8_step(lens, Hq, Hkv, D, page, seed):
+    """A decode step over an fp8 cache: the bf16 cache of the same seed
+    quantised with per-(layer, kv head) scales (by the oracle's store)."""
+    st = W.make_decode_step(lens=lens, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, n_layers=2, size=128,
+                            page_size=page, seed=seed, layer=1, req_rows=len(lens) + 3, max_ctx=max(lens) + 5)
+    kb, vb = _fill_new_token(st)
+    rng = np.random.default_rng(seed)
+    ks = (rng.uniform(0.5, 2.0, (2, Hkv)) / 112).astype(np.float32)
+    vs = (rng.uniform(0.5, 2.0, (2, Hkv)) / 112).astype(np.float32)
+    k8 = oracle.f32_to_e4m3(oracle.bf16_to_f64(kb).astype(np.float32) / ks[:, None, :, None])
+    v8 = oracle.f32_to_e4m3(oracle.bf16_to_f64(vb).astype(np.float32) / vs[:, None, :, None])
+    return st, k8, v8, ks, vs
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,page,lens", [
+    (4, 4, 8, 4, [5, 1, 9]), (8, 2, 16, 1, [13, 7]), (16, 2, 32, 16, [40, 17])])
+def test_decode_fp8_matches_library_sdpa_on_dequantised_cache(Hq, Hkv, D, page, lens):
+    st, k8, v8, ks, vs = _fp8_step(lens, Hq, Hkv, D, page, seed=sum(lens) + D)
+    out = oracle.decode_fp8(bits(st.q), k8, v8, 1, st.kv.req_to_token.numpy(), st.kv.req_pool_indices.numpy(),
+                            st.kv.seq_lens.numpy(), st.scale, ks, vs)
+    kf = _torch_e4m3_values(k8) * ks[:, None, :, None].astype(np.float64)
+    vf = _torch_e4m3_values(v8) * vs[:, None, :, None].astype(np.float64)
+    qf = oracle.bf16_to_f64(bits(st.q))
+    G = Hq // Hkv
+    for b, n in enumerate(lens):
+        slots = st.kv.req_to_token[int(st.kv.req_pool_indices[b]), :n].numpy()
+        for hq in range(Hq):
+            ref = _sdpa_f64(qf[b, hq][None], kf[1, slots, hq // G], vf[1, slots, hq // G], st.scale)
+            np.testing.assert_allclose(out[b, hq], ref[0], rtol=1e-12, atol=1e-12)
+
+
+def test_decode_fp8_with_power_of_two_scales_equals_bf16_decode():
+    # e4m3 values times 2^k are bf16 numbers, so the bf16 oracle on the
+    # dequantised cache computes the same attention
+    st, k8, v8, _, _ = _fp8_step([11, 30], 8, 2, 16, 4, seed=5)
+    ks = np.array([[2.0 ** -5, 2.0 ** -7], [2.0 ** -6, 2.0 ** -4]], np.float32)
+    vs = np.array([[2.0 ** -3, 1.0], [2.0 ** -8, 2.0 ** -6]], np.float32)
+    kbf = oracle.f64_to_bf16(oracle.e4m3_to_f64(k8) * ks[:, None, :, None])
+    vbf = oracle.f64_to_bf16(oracle.e4m3_to_f64(v8) * vs[:, None, :, None])
+    args = (st.kv.req_to_token.numpy(), st.kv.req_pool_indices.numpy(), st.kv.seq_lens.numpy(), st.scale)
+    ref = oracle.decode(bits(st.q), kbf, vbf, 1, *args)
+    out = oracle.decode_fp8(bits(st.q), k8, v8, 1, *args, ks, vs)
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-15)
