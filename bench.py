@@ -70,6 +70,7 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--only-main", action="store_true", help="skip the secondary workloads")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--no-fp8", action="store_true", help="skip the sweep over an e4m3 copy of the cache")
     p.add_argument("--profile", choices=["decode", "prefill", "rope", "store"], default=None,
                    help="run a small fixed case of one kernel (for ncu captures) and exit")
     return p.parse_args()
@@ -221,6 +222,49 @@ def decode_bytes(n, Hq=HQ, Hkv=HKV, Dh=D):
     """Algorithmic bytes of one decode call for one request of n tokens:
     K+V rows, req_to_token entries, q in, out back, request metadata."""
     return n * Hkv * Dh * 2 * 2 + n * 4 + Hq * Dh * 2 * 2 + 8
+
+
+def decode_bytes_fp8(n, Hq=HQ, Hkv=HKV, Dh=D):
+    """As decode_bytes over an e4m3 cache: one byte per K/V element, plus
+    the head's two fp32 scales."""
+    return n * Hkv * Dh * 2 + n * 4 + Hq * Dh * 2 * 2 + 8 + Hkv * 2 * 4
+
+
+def fp8_sweep(sw, peaks, s):
+    """The decode sweep's contexts over an e4m3 copy of the same cache (one
+    scale per layer and kv head, quantised by the library's store), timed
+    the same way: the 32-layer rotation captured per context."""
+    from paged_kv_cache_188_gb300 import api
+    kv = sw.kv
+    n_layers, size = kv.k_buf.shape[0], kv.k_buf.shape[1]
+    k8 = torch.empty(kv.k_buf.shape, dtype=torch.uint8, device=sw.dev)
+    v8 = torch.empty_like(k8)
+    ks = torch.full((n_layers, HKV), 4.5 / 448, dtype=torch.float32, device=sw.dev)
+    vs = ks.clone()
+    loc = torch.arange(size, dtype=torch.int32, device=sw.dev)
+    for l in range(n_layers):
+        api.pa_kv_store_fp8(k8, v8, l, kv.k_buf[l], kv.v_buf[l], loc, ks, vs, sw.err, stream=s)
+    torch.cuda.synchronize()
+    per, b_tot, ms_tot = [], 0.0, 0.0
+    for p, n in enumerate(SWEEP):
+        def call(p=p):
+            for l in range(N_LAYERS):
+                api.pa_paged_decode_attn_fp8(sw.q[p, l], k8, v8, l, kv.req_to_token, kv.req_pool_indices,
+                                             sw.seq[p], sw.scale, ks, vs, sw.ws, MAX_SPLITS, sw.out[p, l], stream=s)
+        g = capture(call, s)
+        g.replay()
+        ms = time_graph(g, 20, s) / N_LAYERS
+        b = decode_bytes_fp8(n)
+        b_tot += b
+        ms_tot += ms
+        per.append({"seq_len": n, "us_per_layer": round(ms * 1e3, 3), "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                    "frac_of_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)})
+    gbs = b_tot / (ms_tot * 1e-3) / 1e9
+    del k8, v8
+    return {"workload": "the decode sweep (B=1, Hq=32 Hkv=8 D=128, 32-layer rotation, contexts 1K-32K) over an "
+                        "e4m3 KV cache [32, 65536, 8, 128] with per-(layer, kv head) scales",
+            "per_context": per, "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "bytes": "algorithmic: 1 byte per K/V element + q/out + page-table entries + scales"}
 
 
 def rope_bytes(T, Hq=HQ, Hkv=HKV, Dh=D):
@@ -417,6 +461,11 @@ def run_ours(args, rank, world, local):
     line["clocks"] = clk.summary()
     if not args.only_main:
         line.update(secondary_workloads(dev, peaks, s))
+    if not args.no_fp8:
+        try:
+            line["decode_fp8"] = fp8_sweep(sw, peaks, s)
+        except Exception as e:   # reported, never fatal to the main line
+            line["decode_fp8"] = {"unavailable": f"{type(e).__name__}: {e}"}
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(sw)
     del sw

@@ -226,6 +226,43 @@ pa_status pa_paged_decode_attn_noalloc(const void *q, int batch, int n_q_heads, 
                                        float scale, int max_splits, void *out, int32_t *error_word,
                                        cudaStream_t st);
 
+/* ------------------------------------------------------- fp8 (e4m3) cache
+ * Commit e58a728 (docs/developer/architecture.md) names an fp8 test among the
+ * CUDA kernel sources and says nothing else about fp8; the scheme is this
+ * library's reading.  An fp8 cache holds each K/V element as one OCP E4M3
+ * byte (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest finite
+ * 448; S.1111.111 is NaN) in uint8 buffers [n_layers, size, n_kv_heads,
+ * head_dim].  k_scale and v_scale are fp32 [n_layers, n_kv_heads] device
+ * arrays owned by the caller (static, per-head calibration is the caller's
+ * business); element x of kv head h in layer l is stored as
+ *     byte = e4m3( fp32(x) / scale[l, h] )   (IEEE fp32 division; round to
+ *            nearest, ties to even; finite overflow saturates to +-448)
+ * and read back as e4m3_value(byte) * scale[l, h].
+ *
+ * pa_kv_store_fp8: as pa_kv_store, quantising.  k_new / v_new bf16
+ * [n_tokens, n_kv_heads, head_dim]; head_dim a multiple of 16; buffers 16-byte
+ * aligned.  Same location checks and error word as pa_kv_store. */
+pa_status pa_kv_store_fp8(void *k_buf, void *v_buf, pa_kv_shape s, int layer_id, const void *k_new,
+                          const void *v_new, const int32_t *loc, int n_tokens, const float *k_scale,
+                          const float *v_scale, int32_t *error_word, cudaStream_t st);
+
+/* pa_paged_decode_attn_fp8: pa_paged_decode_attn over an fp8 cache -- the
+ * same arguments, workspace, split plan, limits and error reporting, plus the
+ * two scale arrays; k_buf / v_buf are the uint8 buffers.  Key j of kv head h
+ * is e4m3_value(K[layer_id, slot_j, h, :]) * k_scale[layer_id, h], value rows
+ * likewise with v_scale.  Rows move as 16-byte cp.async copies.  The dot
+ * products run on f16 tensor-core MMAs with fp32 accumulation: q is rounded
+ * to f16 (exact for bf16 values of magnitude 2^-14 .. 65504; larger ones are
+ * clamped to +-65504), keys and values are exact in f16, the softmax weights
+ * are rounded to f16. */
+pa_status pa_paged_decode_attn_fp8(const void *q, int batch, int n_q_heads, const void *k_buf,
+                                   const void *v_buf, pa_kv_shape s, int layer_id,
+                                   const int32_t *req_to_token, int req_rows, int max_ctx,
+                                   const int32_t *req_pool_indices, const int32_t *seq_lens,
+                                   float scale, const float *k_scale, const float *v_scale,
+                                   void *workspace, size_t workspace_bytes, int max_splits, void *out,
+                                   cudaStream_t st);
+
 /* ------------------------------------------------------ fused decode step
  * One layer's decode step in one launch (commit 398e8a3: the CUDA-graph
  * decode step over packed inputs, rotary embedding on packed 3-D inputs, K/V

@@ -48,7 +48,7 @@ EXPORTS = ["pa_status_string", "pa_decode_workspace_bytes", "pa_prefill_workspac
            "pa_paged_decode_attn", "pa_paged_prefill_attn", "pa_paged_decode_attn_noalloc",
            "pa_set_launch_overlap", "pa_get_launch_overlap", "pa_decode_step",
            "pa_paged_prefill_attn_last", "pa_dense_prefill_attn", "pa_cascade_workspace_bytes",
-           "pa_paged_decode_attn_cascade"]
+           "pa_paged_decode_attn_cascade", "pa_kv_store_fp8", "pa_paged_decode_attn_fp8"]
 
 _lib = None
 
@@ -88,6 +88,9 @@ def lib():
     L.pa_cascade_workspace_bytes.argtypes = [CascadeCaps, i32, i32, i32]
     L.pa_paged_decode_attn_cascade.argtypes = [P, i32, i32, P, P, KvShape, i32, P, i32, i32, P, P, P, P, P, i32,
                                                CascadeCaps, f32, P, sz, P, P]
+    L.pa_kv_store_fp8.argtypes = [P, P, KvShape, i32, P, P, P, i32, P, P, P, P]
+    L.pa_paged_decode_attn_fp8.argtypes = [P, i32, i32, P, P, KvShape, i32, P, i32, i32, P, P, f32, P, P, P, sz,
+                                           i32, P, P]
     L.pa_set_launch_overlap.argtypes = [i32]
     L.pa_get_launch_overlap.argtypes = []
     for name in EXPORTS[3:]:
@@ -127,6 +130,25 @@ def _kv_shape(k_buf, v_buf):
     _need(v_buf, torch.bfloat16, "v_buf", 4)
     if k_buf.shape != v_buf.shape:
         raise ValueError("k_buf and v_buf shapes differ")
+    return KvShape(*k_buf.shape)
+
+
+FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def _kv_shape_fp8(k_buf, v_buf, k_scale, v_scale):
+    """An e4m3 cache: uint8 (or float8_e4m3fn) [n_layers, size, Hkv, D] buffers
+    and fp32 [n_layers, Hkv] scales."""
+    for t, name in ((k_buf, "k_buf"), (v_buf, "v_buf")):
+        if t.dtype not in FP8_DTYPES:
+            raise TypeError(f"{name} must be uint8 or float8_e4m3fn, got {t.dtype}")
+        _need(t, t.dtype, name, 4)
+    if k_buf.shape != v_buf.shape:
+        raise ValueError("k_buf and v_buf shapes differ")
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(v_scale, torch.float32, "v_scale", 2)
+    if tuple(k_scale.shape) != tuple(k_buf.shape[:1] + k_buf.shape[2:3]) or v_scale.shape != k_scale.shape:
+        raise ValueError("k_scale / v_scale must be [n_layers, n_kv_heads]")
     return KvShape(*k_buf.shape)
 
 
@@ -189,6 +211,22 @@ def pa_kv_store(k_buf, v_buf, layer_id, k_new, v_new, loc, error_word=None, stre
                                          _p(error_word), _stream(stream)))
 
 
+def pa_kv_store_fp8(k_buf, v_buf, layer_id, k_new, v_new, loc, k_scale, v_scale, error_word=None, stream=None):
+    """Quantising KV store into an e4m3 cache (bf16 rows divided by their
+    (layer, kv head) scale, rounded to e4m3)."""
+    s = _kv_shape_fp8(k_buf, v_buf, k_scale, v_scale)
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(loc, torch.int32, "loc", 1)
+    T = loc.numel()
+    if tuple(k_new.shape) != (T, s.n_kv_heads, s.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [n_tokens, n_kv_heads, head_dim]")
+    if error_word is not None:
+        _need(error_word, torch.int32, "error_word")
+    _ok("pa_kv_store_fp8", lib().pa_kv_store_fp8(_p(k_buf), _p(v_buf), s, layer_id, _p(k_new), _p(v_new), _p(loc),
+                                                 T, _p(k_scale), _p(v_scale), _p(error_word), _stream(stream)))
+
+
 def pa_rope_packed(q, k, positions, cos_tab, sin_tab, error_word=None, stream=None):
     _need(q, torch.bfloat16, "q", 3)
     _need(positions, torch.int32, "positions", 1)
@@ -225,6 +263,25 @@ def pa_paged_decode_attn(q, k_buf, v_buf, layer_id, req_to_token, req_pool_indic
         _p(q), B, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(req_to_token), req_to_token.shape[0],
         req_to_token.shape[1], _p(req_pool_indices), _p(seq_lens), float(scale), _p(workspace),
         workspace.numel(), max_splits, _p(out), _stream(stream)))
+
+
+def pa_paged_decode_attn_fp8(q, k_buf, v_buf, layer_id, req_to_token, req_pool_indices, seq_lens, scale,
+                             k_scale, v_scale, workspace, max_splits, out, stream=None):
+    """Decode attention over an e4m3 cache with per-(layer, kv head) scales."""
+    s = _kv_shape_fp8(k_buf, v_buf, k_scale, v_scale)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(req_to_token, torch.int32, "req_to_token", 2)
+    _need(req_pool_indices, torch.int32, "req_pool_indices", 1)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(workspace, torch.uint8, "workspace")
+    B, Hq, D = q.shape
+    if out.shape != q.shape or D != s.head_dim or req_pool_indices.numel() != B or seq_lens.numel() != B:
+        raise ValueError("q/out [batch, n_q_heads, head_dim], req_pool_indices/seq_lens [batch] expected")
+    _ok("pa_paged_decode_attn_fp8", lib().pa_paged_decode_attn_fp8(
+        _p(q), B, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(req_to_token), req_to_token.shape[0],
+        req_to_token.shape[1], _p(req_pool_indices), _p(seq_lens), float(scale), _p(k_scale), _p(v_scale),
+        _p(workspace), workspace.numel(), max_splits, _p(out), _stream(stream)))
 
 
 def pa_decode_step(q, k_new, v_new, positions, cos_tab, sin_tab, k_buf, v_buf, layer_id, loc, req_to_token,

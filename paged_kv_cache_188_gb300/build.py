@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libpagedattn.so")
-SOURCES = ["pa_api.cu", "pa_store_rope.cu", "pa_decode.cu", "pa_decode_step.cu", "pa_decode_cascade.cu", "pa_prefill.cu"]
+SOURCES = ["pa_api.cu", "pa_store_rope.cu", "pa_decode.cu", "pa_decode_step.cu", "pa_decode_cascade.cu",
+           "pa_decode_fp8.cu", "pa_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
                      "--expt-relaxed-constexpr", "-I" + INCLUDE, "-I" + CSRC]

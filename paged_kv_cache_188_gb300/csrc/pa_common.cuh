@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -54,6 +56,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D[16x8] += A[16x16] * B[16x8], f16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // transpose an 8x8 b16 matrix held one 32-bit pair per thread (mma fragment layout)
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
 {
@@ -95,6 +107,45 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// two fp32 -> packed f16x2 (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Two e4m3 bytes (the low one first) -> f16x2 (the low byte's value in the low
+// half).  Exact: every e4m3 value is an f16 number.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// bf16x2 word -> f16x2 word, each value clamped to the f16 range first (f16
+// holds bf16's 8 significant bits; magnitudes below 2^-14 lose low bits).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t w)
+{
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+    return pack_f16x2(fminf(fmaxf(lo, -65504.f), 65504.f), fminf(fmaxf(hi, -65504.f), 65504.f));
+}
+
+// Sixteen fp32 values x[i] / scale (IEEE division) -> e4m3 bytes, round to
+// nearest even, finite overflow saturating to +-448; x[0] in the low byte.
+__device__ __forceinline__ uint4 quant_e4m3x16(const float (&x)[16], float scale)
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __nv_fp8x2_storage_t a = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(x[4 * i], scale), __fdiv_rn(x[4 * i + 1], scale)), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t b = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(x[4 * i + 2], scale), __fdiv_rn(x[4 * i + 3], scale)), __NV_SATFINITE, __NV_E4M3);
+        w[i] = (uint32_t)a | ((uint32_t)b << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Rotate one interleaved bf16 pair (x0, x1) stored as a 32-bit word by the

@@ -48,6 +48,15 @@
 //    in registers as it is loaded, and the CTA holding the last split of a
 //    (request, kv head) writes that head's new K (rotated) and V rows at
 //    loc[b] before it loads any tile; it is the only CTA that reads them.
+//  * fp8 cache (MODE_FP8, pa_paged_decode_attn_fp8): K/V rows are D bytes of
+//    e4m3 with one scale per (layer, kv head).  Rows reach the ring by
+//    cp.async only.  Keys feed f16 MMAs straight from shared memory: lane t4
+//    takes bytes [t4 D/4, (t4+1) D/4) of rows g and g+8, four per k-step, so
+//    the head dimension is permuted inside the dot product and q is loaded in
+//    the same order (as f16).  Values are widened to f16 into a per-warp
+//    staging tile in the bf16 tile layout and read by the same transposing
+//    ldmatrix.  The K scale joins the softmax scale; the V scale multiplies
+//    the item's output state.
 //  * Launched behind another kernel (launch overlap on), the CTA waits for it
 //    at the start, or -- early-metadata mode -- after planning and the first
 //    page-table reads, just before its first K/V load.
@@ -76,14 +85,21 @@ constexpr int kDecMaxSplits = 128;
 // normalised output and log-sum-exp; SUFFIX runs every request over its
 // tokens after its group's prefix and folds the prefix result into its
 // output by log-sum-exp.
-enum DecMode { MODE_PLAIN = 0, MODE_FUSED = 1, MODE_PREFIX = 2, MODE_SUFFIX = 3 };
+// FP8: decode attention over an e4m3 cache.
+enum DecMode { MODE_PLAIN = 0, MODE_FUSED = 1, MODE_PREFIX = 2, MODE_SUFFIX = 3, MODE_FP8 = 4 };
 
 struct DecodeArgs {
     CUtensorMap tm_k;    // 2-D (element, row) over k_buf rows, 64 x 16 boxes, 128-byte swizzle
     CUtensorMap tm_v;
     const __nv_bfloat16 *q;
-    const __nv_bfloat16 *k_layer;
-    const __nv_bfloat16 *v_layer;
+    union {   // the layer's K / V rows: bf16, or e4m3 bytes in FP8 mode
+        const __nv_bfloat16 *k_layer;
+        const uint8_t *k8_layer;
+    };
+    union {
+        const __nv_bfloat16 *v_layer;
+        const uint8_t *v8_layer;
+    };
     const int32_t *req_to_token;
     const int32_t *req_pool_indices;
     const int32_t *seq_lens;
@@ -104,8 +120,14 @@ struct DecodeArgs {
     const __nv_bfloat16 *v_new;
     const int32_t *positions;
     const int32_t *loc;
-    const float *cos_tab;
-    const float *sin_tab;
+    union {   // fused step: the RoPE tables; FP8: the layer's per-kv-head K / V scales [Hkv]
+        const float *cos_tab;
+        const float *k_scale;
+    };
+    union {
+        const float *sin_tab;
+        const float *v_scale;
+    };
     __nv_bfloat16 *k_layer_w;   // the layer's K / V rows, writable
     __nv_bfloat16 *v_layer_w;
     int max_pos;
@@ -165,12 +187,14 @@ __device__ __forceinline__ float ex2(float x)
 // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)) -- the
 // layout TMA writes and the cp.async path reproduces; consumer scratch;
 // per-warp stage validity masks and mbarriers; the plan's prefix array.
-template <int D, int S, int NH>
+template <int D, int S, int NH, bool F8 = false>
 struct DecSmem {
     static constexpr int kHalf = kDecTile * 128;                         // 16 rows x 128 B
-    static constexpr int kTile = (D / 64) * kHalf;                       // one K or V tile
+    static constexpr int kTile16 = (D / 64) * kHalf;                     // one K or V tile of 16-bit values
+    static constexpr int kTile = F8 ? kDecTile * D : kTile16;            // one K or V tile as loaded
     static constexpr int kStage = 2 * kTile;
-    static constexpr int kRing = S * kStage;                             // per warp
+    static constexpr int kStaging = F8 ? kTile16 : 0;                    // fp8: the V tile widened to f16
+    static constexpr int kRing = S * kStage + kStaging;                  // per warp
     static constexpr int kScratchOff = kDecWarps * kRing;
     // half the warps' O states [4][G][D + 4] fp32 at a time, later the split merge
     // [sb][G][2] + [sb][G] + [G]
@@ -186,6 +210,12 @@ struct DecSmem {
     __device__ static __forceinline__ uint32_t off(int r, int c)
     {
         return (uint32_t)((c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    }
+    // fp8 tiles: row r of D bytes, 16-byte chunk c (128-byte rows XOR-swizzled
+    // like off; 64-byte rows plain -- both conflict free for the fragment reads)
+    __device__ static __forceinline__ uint32_t off8(int r, int c)
+    {
+        return D == 128 ? (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)) : (uint32_t)(r * D + (c << 4));
     }
 };
 constexpr size_t kSmemLimit = 232448 - 4096;   // opt-in maximum minus static shared memory (with margin)
@@ -237,7 +267,7 @@ __device__ __forceinline__ void req_span(const DecodeArgs &a, int b, int &start,
 template <int MODE>
 __device__ __forceinline__ int req_len(const DecodeArgs &a, int b)
 {
-    if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED) {
+    if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8) {
         return clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
     } else {
         int start, n, row;
@@ -255,7 +285,7 @@ __device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pr
     const int local = item - s_pref[lo];
     I.s = local / a.Hkv;
     I.h = local - I.s * a.Hkv;
-    if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED) {
+    if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8) {
         int n = clamp_len(__ldg(a.seq_lens + lo), a.max_ctx);
         int len;
         split_of(n, chunk, a.max_splits, I.sb, len);
@@ -285,8 +315,9 @@ __device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pr
 template <int D, int S, int NH, int MODE>
 __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __grid_constant__ DecodeArgs a)
 {
-    using L = DecSmem<D, S, NH>;
+    using L = DecSmem<D, S, NH, MODE == MODE_FP8>;
     constexpr bool FUSED = MODE == MODE_FUSED;
+    constexpr bool F8 = MODE == MODE_FP8;
     // the suffix launch plans from req_start, which the prefix launch writes:
     // it never plans before its wait
     const bool early = a.early_meta && MODE != MODE_SUFFIX;
@@ -417,6 +448,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         const bool ok = in_range && sl >= 0 && sl < a.size;
         if (!ok) sl = -1;
         const unsigned vmask = __ballot_sync(0xffffffffu, ok);
+        if constexpr (F8) {
+            // D-byte rows, D/16 lanes per row; masked rows zero-filled, not read
+            constexpr int CPR8 = D / 16, TPI8 = 32 / CPR8;
+            if (lane == 0) {
+                s_vmask[warp * S + st] = vmask;
+                mbar_arrive_expect_tx(fb, 0u);
+            }
+            __syncwarp();
+            const uint8_t *kh = a.k8_layer + (int64_t)cur.I.h * D;
+            const uint8_t *vh = a.v8_layer + (int64_t)cur.I.h * D;
+#pragma unroll
+            for (int j = 0; j < kDecTile / TPI8; ++j) {
+                const int r = j * TPI8 + lane / CPR8;
+                const int ch = lane % CPR8;
+                const int rs = __shfl_sync(0xffffffffu, sl, r);
+                const int64_t off = rs >= 0 ? (int64_t)rs * slot_stride + ch * 16 : 0;
+                const int nb = rs >= 0 ? 16 : 0;
+                cp_async_16(kb + L::off8(r, ch), kh + off, nb);
+                cp_async_16(vb + L::off8(r, ch), vh + off, nb);
+            }
+        } else {
         // 16 tokens on 16 consecutive slots (one page): four TMA boxes
         const int s0 = __shfl_sync(0xffffffffu, sl, 0);
         const bool page = (__ballot_sync(0xffffffffu, ok && sl == s0 + lane) & 0xFFFFu) == 0xFFFFu;
@@ -448,6 +500,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 cp_async_16(kb + o, kh + off, nb);
                 cp_async_16(vb + o, vh + off, nb);
             }
+        }
         }
         cp_async_arrive_noinc(fb);
         ++n_issued;
@@ -659,7 +712,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         for (int k = 0; k < EPT; ++k) {
             const int e = tid + k * kDecThreads;
             if (e >= G * D) continue;
-            if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED) {
+            if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8) {
                 const float lt = s_lt[e / D];
                 a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc[k] / lt : 0.f);
             } else {
@@ -693,7 +746,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             // row is RoPE pair i, rotated by table row positions[b]
             // (prefix launch: row hd of a virtual request is head hd % G of
             // member hd / G of its chunk, G the real GQA group)
-            if constexpr (MODE != MODE_PREFIX) {
+            if constexpr (F8) {
+                // the keys' permuted head dimension: k-step kk of lane t4
+                // covers d = t4 * D/4 + 4 kk + {0, 1 | 2, 3}; q as f16
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt) {
+                        const int hd = nt * 8 + g;
+                        const int w = t4 * (D / 8) + 2 * kk;
+                        qb[kk][nt][0] = hd < G ? __ldg(q32 + hd * (D / 2) + w) : 0u;
+                        qb[kk][nt][1] = hd < G ? __ldg(q32 + hd * (D / 2) + w + 1) : 0u;
+                    }
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt) {
+                        qb[kk][nt][0] = bf16x2_to_f16x2_sat(qb[kk][nt][0]);
+                        qb[kk][nt][1] = bf16x2_to_f16x2_sat(qb[kk][nt][1]);
+                    }
+            } else if constexpr (MODE != MODE_PREFIX) {
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk)
 #pragma unroll
@@ -762,6 +834,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
 #pragma unroll
         for (int nt = 0; nt < NH; ++nt) m[nt][0] = m[nt][1] = -INFINITY, l[nt][0] = l[nt][1] = 0.f;
 
+        float sl2_f8 = 0.f;   // fp8: softmax scale (log2 units) times the head's K scale
+        if constexpr (F8) sl2_f8 = a.scale_log2 * __ldg(a.k_scale + I.h);
         for (int i = warp; i < I.ntiles; i += kDecWarps) {
             if (!bad) issue();
             const int st = n_done % S;
@@ -777,7 +851,39 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
                 sc2[nt][0] = sc2[nt][1] = sc2[nt][2] = sc2[nt][3] = 0.f;
             }
-            {
+            if constexpr (F8) {
+                // A fragments straight from the e4m3 rows g and g + 8: lane t4
+                // holds bytes [t4 D/4, (t4+1) D/4) of each, four per k-step
+                constexpr int F8CH = D / 64;
+                uint32_t kw[2][KSTEPS];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                    for (int j = 0; j < F8CH; ++j) {
+                        const uint4 v = ld_shared_v4(kb + L::off8(g + 8 * rr, t4 * F8CH + j));
+                        kw[rr][4 * j] = v.x;
+                        kw[rr][4 * j + 1] = v.y;
+                        kw[rr][4 * j + 2] = v.z;
+                        kw[rr][4 * j + 3] = v.w;
+                    }
+#pragma unroll
+                for (int kk = 0; kk < KSTEPS; ++kk) {
+                    uint32_t af[4];
+                    af[0] = e4m3x2_to_f16x2(kw[0][kk]);
+                    af[1] = e4m3x2_to_f16x2(kw[1][kk]);
+                    af[2] = e4m3x2_to_f16x2(kw[0][kk] >> 16);
+                    af[3] = e4m3x2_to_f16x2(kw[1][kk] >> 16);
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt) {
+                        if (kk & 1) mma_f16_16816(sc2[nt], af, qb[kk][nt][0], qb[kk][nt][1]);
+                        else mma_f16_16816(sc[nt], af, qb[kk][nt][0], qb[kk][nt][1]);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[nt][e] += sc2[nt][e];
+            } else {
                 const int r = ((lane >> 3) & 1) * 8 + (lane & 7);
                 const int c_hi = lane >> 4;
 #pragma unroll
@@ -800,10 +906,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             float mr[NH][2], al[NH][2];
 #pragma unroll
             for (int nt = 0; nt < NH; ++nt) {
+                if constexpr (F8) {
+                    sc[nt][0] = ok0 ? sc[nt][0] * sl2_f8 : -INFINITY;
+                    sc[nt][1] = ok0 ? sc[nt][1] * sl2_f8 : -INFINITY;
+                    sc[nt][2] = ok1 ? sc[nt][2] * sl2_f8 : -INFINITY;
+                    sc[nt][3] = ok1 ? sc[nt][3] * sl2_f8 : -INFINITY;
+                } else {
                 sc[nt][0] = ok0 ? sc[nt][0] * a.scale_log2 : -INFINITY;
                 sc[nt][1] = ok0 ? sc[nt][1] * a.scale_log2 : -INFINITY;
                 sc[nt][2] = ok1 ? sc[nt][2] * a.scale_log2 : -INFINITY;
                 sc[nt][3] = ok1 ? sc[nt][3] * a.scale_log2 : -INFINITY;
+                }
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     float v = fmaxf(sc[nt][j], sc[nt][j + 2]);
@@ -826,8 +939,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 const float p3 = ex2(sc[nt][3] - mr[nt][1]);
                 l[nt][0] = l[nt][0] * al[nt][0] + (p0 + p2);
                 l[nt][1] = l[nt][1] * al[nt][1] + (p1 + p3);
+                if constexpr (F8) {
+                    pb[nt][0] = movmatrix_trans(pack_f16x2(p0, p1));
+                    pb[nt][1] = movmatrix_trans(pack_f16x2(p2, p3));
+                } else {
                 pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
                 pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+                }
             }
 #pragma unroll
             for (int dm = 0; dm < DM; ++dm)
@@ -839,7 +957,32 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                     o[dm][nt][3] *= al[nt][1];
                 }
             // O^T += V^T P^T: V^T fragments by transposing ldmatrix of the V rows
-            {
+            if constexpr (F8) {
+                // widen the e4m3 V tile to f16 in the warp's staging tile (bf16
+                // tile layout); the staging was last read before the previous
+                // tile's closing __syncwarp
+                constexpr int CPR8 = D / 16;
+                const uint32_t stg = ring + S * L::kStage;
+#pragma unroll
+                for (int j = 0; j < kDecTile * CPR8 / 32; ++j) {
+                    const int qc = j * 32 + lane, r = qc / CPR8, c = qc % CPR8;
+                    const uint4 v = ld_shared_v4(vb + L::off8(r, c));
+                    st_shared_v4(stg + L::off(r, 2 * c), e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16),
+                                 e4m3x2_to_f16x2(v.y), e4m3x2_to_f16x2(v.y >> 16));
+                    st_shared_v4(stg + L::off(r, 2 * c + 1), e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16),
+                                 e4m3x2_to_f16x2(v.w), e4m3x2_to_f16x2(v.w >> 16));
+                }
+                __syncwarp();
+                const int r = ((lane >> 4) & 1) * 8 + (lane & 7);
+                const int c_lo = (lane >> 3) & 1;
+#pragma unroll
+                for (int dm = 0; dm < DM; ++dm) {
+                    uint32_t af[4];
+                    ldmatrix_x4_trans(stg + L::off(r, dm * 2 + c_lo), af[0], af[1], af[2], af[3]);
+#pragma unroll
+                    for (int nt = 0; nt < NH; ++nt) mma_f16_16816(o[dm][nt], af, pb[nt][0], pb[nt][1]);
+                }
+            } else {
                 const int r = ((lane >> 4) & 1) * 8 + (lane & 7);
                 const int c_lo = (lane >> 3) & 1;
 #pragma unroll
@@ -853,6 +996,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             __syncwarp();
         }
 
+        if constexpr (F8) {
+            const float vsc = __ldg(a.v_scale + I.h);
+#pragma unroll
+            for (int dm = 0; dm < DM; ++dm)
+#pragma unroll
+                for (int nt = 0; nt < NH; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[dm][nt][e] *= vsc;
+        }
         // ------------------------------------- merge the warps' states
 #pragma unroll
         for (int nt = 0; nt < NH; ++nt)
@@ -929,7 +1081,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             if (e >= G * D) continue;
             const int gg = e / D, d = e - gg * D;
             if (I.sb == 1) {
-                if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED)
+                if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8)
                     a.out[((int64_t)I.b * a.Hq + hq0 + gg) * D + d] =
                         __float2bfloat16_rn(lsum[k] > 0.f ? acc[k] / lsum[k] : 0.f);
                 else
@@ -975,7 +1127,7 @@ template <int D, int S, int NH, int MODE>
 static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
 {
     auto kern = paged_decode_kernel<D, S, NH, MODE>;
-    const size_t smem = DecSmem<D, S, NH>::bytes(a.batch);
+    const size_t smem = DecSmem<D, S, NH, MODE == MODE_FP8>::bytes(a.batch);
     if (smem > kSmemLimit) return PA_ERR_UNSUPPORTED;
     static size_t configured = 0;
     if (smem > configured) {
@@ -991,11 +1143,19 @@ static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
 template <int D, int NH, int MODE>
 static pa_status dispatch_decode(const DecodeArgs &a, cudaStream_t st)
 {
-    if (DecSmem<D, 4, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 4, NH, MODE>(a, st);
-    if (DecSmem<D, 3, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 3, NH, MODE>(a, st);
-    return launch_decode<D, 2, NH, MODE>(a, st);
+    if constexpr (MODE == MODE_FP8) {
+        // stages of half the bytes: a deeper ring keeps as many bytes in flight
+        if (DecSmem<D, 5, NH, true>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 5, NH, MODE>(a, st);
+        if (DecSmem<D, 4, NH, true>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 4, NH, MODE>(a, st);
+        return launch_decode<D, 2, NH, MODE>(a, st);
+    } else {
+        if (DecSmem<D, 4, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 4, NH, MODE>(a, st);
+        if (DecSmem<D, 3, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 3, NH, MODE>(a, st);
+        return launch_decode<D, 2, NH, MODE>(a, st);
+    }
 }
 static_assert(DecSmem<128, 2, 2>::bytes(kDecMaxBatch) <= kSmemLimit, "decode smem at the largest batch");
+static_assert(DecSmem<128, 2, 2, true>::bytes(kDecMaxBatch) <= kSmemLimit, "fp8 decode smem at the largest batch");
 
 
 
@@ -1037,14 +1197,14 @@ static bool fill_decode_args(DecodeArgs &a, const void *q, int batch, int n_q_he
                              const void *v_buf, pa_kv_shape s, int layer_id, const int32_t *req_to_token,
                              int req_rows, int max_ctx, const int32_t *req_pool_indices, const int32_t *seq_lens,
                              float scale, int max_splits, void *out, int32_t *err, const DecodeWsLayout &ws,
-                             unsigned char *wbase)
+                             unsigned char *wbase, bool bf16_cache = true)
 {
     memset(&a, 0, sizeof a);
     const cuuint64_t dims[2] = {(cuuint64_t)s.n_kv_heads * s.head_dim, (cuuint64_t)s.n_layers * s.size};
     const cuuint64_t strides[1] = {(cuuint64_t)s.n_kv_heads * s.head_dim * 2};
     const cuuint32_t box[2] = {64, kDecTile};
-    if (!encode_tmap_bf16(&a.tm_k, k_buf, 2, dims, strides, box) ||
-        !encode_tmap_bf16(&a.tm_v, v_buf, 2, dims, strides, box))
+    if (bf16_cache && (!encode_tmap_bf16(&a.tm_k, k_buf, 2, dims, strides, box) ||
+                       !encode_tmap_bf16(&a.tm_v, v_buf, 2, dims, strides, box)))
         return false;
     a.layer_row0 = layer_id * s.size;
     const int64_t layer_off = (int64_t)layer_id * s.size * s.n_kv_heads * s.head_dim;

@@ -172,3 +172,31 @@ def test_cascade_workspace_and_validation(lib):
     assert call(wsb=small - 1) == 5
     assert call(ip=0) == 1
     assert call(ip=FAKE + 2) == 3
+
+
+def test_fp8_entry_points_host_validation(lib):
+    P = ctypes.c_void_p
+
+    def store(s=None, layer=0, ks=FAKE, vs=FAKE, n=4, k=FAKE):
+        return lib.pa_kv_store_fp8(P(k), P(FAKE), s or _shape(d=64), layer, P(FAKE), P(FAKE), P(FAKE), n,
+                                   P(ks) if ks else None, P(vs) if vs else None, None, None)
+
+    assert store(layer=2) == 2
+    assert store(s=_shape(d=8)) == 4                         # head_dim must be a multiple of 16
+    assert store(ks=0) == 1
+    assert store(vs=FAKE + 2) == 3
+    assert store(k=FAKE + 8) == 3                            # 16-byte aligned buffers
+    assert store(n=0, ks=0, vs=0) == 0                       # no tokens: nothing to do
+
+    def dec(batch=1, ks=FAKE, vs=FAKE, s=None, hq=8):
+        return lib.pa_paged_decode_attn_fp8(
+            P(FAKE), batch, hq, P(FAKE), P(FAKE), s or _shape(), 0, P(FAKE), 1, 16, P(FAKE), P(FAKE), 0.125,
+            P(ks) if ks else None, P(vs) if vs else None, P(FAKE), api.pa_decode_workspace_bytes(1, 8, 2, 64, 4),
+            4, P(FAKE), None)
+
+    assert dec(ks=0) == 1
+    assert dec(vs=FAKE + 1) == 3
+    assert dec(s=_shape(d=96)) == 4
+    assert dec(hq=7) == 2
+    assert dec(batch=2) == 5                                 # workspace sized for one request
+    assert dec(batch=0, ks=0, vs=0) == 0
