@@ -469,38 +469,38 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 cp_async_16(vb + L::off8(r, ch), vh + off, nb);
             }
         } else {
-        // 16 tokens on 16 consecutive slots (one page): four TMA boxes
-        const int s0 = __shfl_sync(0xffffffffu, sl, 0);
-        const bool page = (__ballot_sync(0xffffffffu, ok && sl == s0 + lane) & 0xFFFFu) == 0xFFFFu;
-        if (lane == 0) {
-            s_vmask[warp * S + st] = vmask;
-            mbar_arrive_expect_tx(fb, page ? 2u * L::kTile : 0u);
-        }
-        __syncwarp();
-        const int h = cur.I.h;
-        if (page) {
+            // 16 tokens on 16 consecutive slots (one page): four TMA boxes
+            const int s0 = __shfl_sync(0xffffffffu, sl, 0);
+            const bool page = (__ballot_sync(0xffffffffu, ok && sl == s0 + lane) & 0xFFFFu) == 0xFFFFu;
             if (lane == 0) {
+                s_vmask[warp * S + st] = vmask;
+                mbar_arrive_expect_tx(fb, page ? 2u * L::kTile : 0u);
+            }
+            __syncwarp();
+            const int h = cur.I.h;
+            if (page) {
+                if (lane == 0) {
 #pragma unroll
-                for (int hh = 0; hh < D / 64; ++hh) {
-                    tma_load_2d(kb + hh * L::kHalf, &a.tm_k, h * D + hh * 64, a.layer_row0 + s0, fb);
-                    tma_load_2d(vb + hh * L::kHalf, &a.tm_v, h * D + hh * 64, a.layer_row0 + s0, fb);
+                    for (int hh = 0; hh < D / 64; ++hh) {
+                        tma_load_2d(kb + hh * L::kHalf, &a.tm_k, h * D + hh * 64, a.layer_row0 + s0, fb);
+                        tma_load_2d(vb + hh * L::kHalf, &a.tm_v, h * D + hh * 64, a.layer_row0 + s0, fb);
+                    }
+                }
+            } else {
+                const __nv_bfloat16 *kh = a.k_layer + (int64_t)h * D;
+                const __nv_bfloat16 *vh = a.v_layer + (int64_t)h * D;
+#pragma unroll
+                for (int j = 0; j < kDecTile / TPI; ++j) {
+                    const int r = j * TPI + lane / CPR;
+                    const int ch = lane % CPR;
+                    const int rs = __shfl_sync(0xffffffffu, sl, r);
+                    const int64_t off = rs >= 0 ? (int64_t)rs * slot_stride + ch * 8 : 0;
+                    const int nb = rs >= 0 ? 16 : 0;      // masked rows: zero fill, no read
+                    const uint32_t o = L::off(r, ch);
+                    cp_async_16(kb + o, kh + off, nb);
+                    cp_async_16(vb + o, vh + off, nb);
                 }
             }
-        } else {
-            const __nv_bfloat16 *kh = a.k_layer + (int64_t)h * D;
-            const __nv_bfloat16 *vh = a.v_layer + (int64_t)h * D;
-#pragma unroll
-            for (int j = 0; j < kDecTile / TPI; ++j) {
-                const int r = j * TPI + lane / CPR;
-                const int ch = lane % CPR;
-                const int rs = __shfl_sync(0xffffffffu, sl, r);
-                const int64_t off = rs >= 0 ? (int64_t)rs * slot_stride + ch * 8 : 0;
-                const int nb = rs >= 0 ? 16 : 0;      // masked rows: zero fill, no read
-                const uint32_t o = L::off(r, ch);
-                cp_async_16(kb + o, kh + off, nb);
-                cp_async_16(vb + o, vh + off, nb);
-            }
-        }
         }
         cp_async_arrive_noinc(fb);
         ++n_issued;
@@ -912,10 +912,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                     sc[nt][2] = ok1 ? sc[nt][2] * sl2_f8 : -INFINITY;
                     sc[nt][3] = ok1 ? sc[nt][3] * sl2_f8 : -INFINITY;
                 } else {
-                sc[nt][0] = ok0 ? sc[nt][0] * a.scale_log2 : -INFINITY;
-                sc[nt][1] = ok0 ? sc[nt][1] * a.scale_log2 : -INFINITY;
-                sc[nt][2] = ok1 ? sc[nt][2] * a.scale_log2 : -INFINITY;
-                sc[nt][3] = ok1 ? sc[nt][3] * a.scale_log2 : -INFINITY;
+                    sc[nt][0] = ok0 ? sc[nt][0] * a.scale_log2 : -INFINITY;
+                    sc[nt][1] = ok0 ? sc[nt][1] * a.scale_log2 : -INFINITY;
+                    sc[nt][2] = ok1 ? sc[nt][2] * a.scale_log2 : -INFINITY;
+                    sc[nt][3] = ok1 ? sc[nt][3] * a.scale_log2 : -INFINITY;
                 }
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -943,8 +943,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                     pb[nt][0] = movmatrix_trans(pack_f16x2(p0, p1));
                     pb[nt][1] = movmatrix_trans(pack_f16x2(p2, p3));
                 } else {
-                pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
-                pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+                    pb[nt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+                    pb[nt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
                 }
             }
 #pragma unroll
