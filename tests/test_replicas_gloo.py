@@ -1,0 +1,55 @@
+"""The replica path of bench.py on CPU: two gloo ranks run the same
+rendezvous, barrier and max / sum reductions that the timed region uses
+under NCCL (replicas only: the attention path has no exchange step, so these
+reductions of timings and byte counts are the only collectives)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+
+    import bench
+    r, w, local = bench.dist_setup(None)
+    bench.barrier(w)
+    # ms per step: the slowest rank's time; bytes: every rank's units
+    ms = bench.max_over_ranks(1.5 + rank, w)
+    total = bench.sum_over_ranks(1000.0 * (rank + 1), w)
+    q.put((r, w, local, ms, total))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_timing_and_bytes():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    try:
+        got = sorted(q.get(timeout=120) for _ in procs)
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.kill()
+    assert [p.exitcode for p in procs] == [0, 0]
+    assert got == [(0, 2, 0, 2.5, 3000.0), (1, 2, 1, 2.5, 3000.0)]
+
+
+def test_reference_arm_other_ranks_do_no_work():
+    import bench
+    assert bench.run_reference(None, 1, 2, 1) is None
