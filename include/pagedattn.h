@@ -17,7 +17,9 @@
  * Conventions shared by every call
  *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous
  *     row-major, with 16-byte aligned base addresses.  bf16 data travel as
- *     IEEE bfloat16 (2 bytes), indices as int32, tables and workspaces as fp32.
+ *     IEEE bfloat16 (2 bytes), indices as int32, tables and workspaces as fp32;
+ *     the fp8 entry points' caches as one e4m3 byte per element with fp32
+ *     per-(layer, kv head) scales.
  *   - The library allocates nothing, keeps no per-call state and never
  *     synchronises the stream (pa_get_error excepted).  Work is enqueued on the
  *     given stream; every call except pa_get_error can be captured in a CUDA

@@ -8,7 +8,9 @@ device memory and streams only.
 
 Dtypes follow the pages (AstrAI commit 398e8a3, tests/inference/test_cache.py):
 bf16 activations and KV buffers, int32 page-table / request-row / location
-indices.  Other dtypes are rejected here, before any launch.
+indices; the fp8 entry points take e4m3 caches (uint8 or float8_e4m3fn
+tensors) with fp32 [n_layers, n_kv_heads] scales.  Other dtypes are rejected
+here, before any launch.
 """
 from __future__ import annotations
 
