@@ -143,3 +143,42 @@ def test_decode_fp8_long_context_splits_deterministic_and_empty():
     ref = oracle.decode_fp8(bits(st.q), kh, vh, 0, npy(st.kv.req_to_token), npy(st.kv.req_pool_indices),
                             npy(st.kv.seq_lens), st.scale, npy(ks), npy(vs), sel=(sel_b, sel_h))
     assert_attention_close(npy(out1.float())[sel_b, sel_h], ref, "fp8 decode 30K")
+
+
+@pytest.mark.parametrize("seq_len", [4096, 32768])
+def test_config2_full_size_fp8(seq_len):
+    """The bench's e4m3 sweep configuration: the [32, 65536, 8, 128] cache
+    quantised by the library's store (layer 17), the step's new token stored,
+    B=1 decode with the bench's split cap.  The request's slots are compared
+    byte for byte with the oracle's quantisation of the generator's bf16 rows
+    (compacted on the host, the new row taken from the step's inputs), and the
+    output with the oracle's attention over those bytes."""
+    st = W.config2(seq_len, device="cuda", fill_layers=[17])
+    dev = st.q.device
+    n_layers, size, Hkv, D = st.kv.k_buf.shape
+    ks, vs = _scales(n_layers, Hkv, seq_len)
+    ksd, vsd = ks.to(dev), vs.to(dev)
+    k8 = torch.zeros((n_layers, size, Hkv, D), dtype=torch.uint8, device=dev)
+    v8 = torch.zeros_like(k8)
+    every = torch.arange(size, dtype=torch.int32, device=dev)
+    api.pa_kv_store_fp8(k8, v8, st.layer, st.kv.k_buf[st.layer], st.kv.v_buf[st.layer], every, ksd, vsd)
+    api.pa_kv_store_fp8(k8, v8, st.layer, st.k_new, st.v_new, st.loc, ksd, vsd)
+    out, _ = _decode_fp8(st, k8, v8, ksd, vsd)
+    # host side: the request's rows in sorted-slot order, from generator data only
+    row = int(st.kv.req_pool_indices[0])
+    slots = st.kv.req_to_token[row, :seq_len].long()
+    uniq, inv = torch.unique(slots, return_inverse=True)
+    kb = bits(st.kv.k_buf[st.layer][uniq])
+    vb = bits(st.kv.v_buf[st.layer][uniq])
+    new = int(inv[seq_len - 1])
+    kb[new], vb[new] = bits(st.k_new)[0], bits(st.v_new)[0]
+    U = uniq.numel()
+    l_ks, l_vs = npy(ks)[st.layer][None], npy(vs)[st.layer][None]
+    kh, vh = oracle.kv_store_fp8(np.zeros((1, U, Hkv, D), np.uint8), np.zeros((1, U, Hkv, D), np.uint8), 0,
+                                 kb, vb, np.arange(U, dtype=np.int32), l_ks, l_vs)
+    _assert_bytes_equal(npy(k8[st.layer][uniq]), kh[0], "K rows of the request")
+    _assert_bytes_equal(npy(v8[st.layer][uniq]), vh[0], "V rows of the request")
+    r2t = npy(inv).astype(np.int32)[None]
+    ref = oracle.decode_fp8(bits(st.q), kh, vh, 0, r2t, np.zeros(1, np.int32), np.array([seq_len], np.int32),
+                            st.scale, l_ks, l_vs)
+    assert_attention_close(npy(out.float()), ref, f"fp8 config 2 seq {seq_len}")
