@@ -200,3 +200,16 @@ def test_fp8_entry_points_host_validation(lib):
     assert dec(hq=7) == 2
     assert dec(batch=2) == 5                                 # workspace sized for one request
     assert dec(batch=0, ks=0, vs=0) == 0
+
+
+def test_fp8_wrappers_reject_wrong_cache_dtypes_before_the_library():
+    import torch
+    bf = torch.zeros((1, 4, 1, 64), dtype=torch.bfloat16)
+    sc = torch.ones((1, 1), dtype=torch.float32)
+    with pytest.raises(TypeError, match="uint8 or float8_e4m3fn"):
+        api.pa_kv_store_fp8(bf, bf, 0, None, None, None, sc, sc)
+    with pytest.raises(TypeError, match="uint8 or float8_e4m3fn"):
+        api.pa_paged_decode_attn_fp8(None, bf, bf, 0, None, None, None, 0.1, sc, sc, None, 4, None)
+    u8 = torch.zeros((1, 4, 1, 64), dtype=torch.uint8)
+    with pytest.raises(TypeError, match="CUDA tensor"):            # host memory is never passed down
+        api.pa_kv_store_fp8(u8, u8, 0, None, None, None, sc, sc)
