@@ -397,6 +397,19 @@ def _torch_e4m3_values(codes: np.ndarray) -> np.ndarray:
         torch.float64).numpy()
 
 
+def test_e4m3_golden(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "e4m3_hand.json")))
+    for c in g["decode"]:
+        got = float(oracle.e4m3_to_f64(np.array([int(c["code"], 16)], np.uint8))[0])
+        if c["value"] == "nan":
+            assert math.isnan(got), c
+        else:
+            assert got == c["value"] and math.copysign(1, got) == math.copysign(1, c["value"]), (c, got)
+    for c in g["encode"]:
+        got = int(oracle.f32_to_e4m3(np.array([c["value"]], np.float32))[0])
+        assert got == int(c["code"], 16), (c, hex(got))
+
+
 def test_e4m3_values_match_torch_for_every_code():
     codes = np.arange(256, dtype=np.uint8)
     ours = oracle.e4m3_to_f64(codes)
