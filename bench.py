@@ -57,8 +57,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, valid only while the kernel source is unchanged (sha256 prefix).
-NCU_TRAFFIC = {"decode": {"sha": "5d3acc4d2afe6e0a", "ratio": round((537.539584 + 2.984192) / 537.460768, 5),
-                          "capture": "ncu, 4 x 32K tokens, one layer: dram read+write 540.52 MB for "
+NCU_TRAFFIC = {"decode": {"sha": "94c99dd8891330fa", "ratio": round((537.53856 + 3.112192) / 537.460768, 5),
+                          "capture": "ncu, 4 x 32K tokens, one layer: dram read+write 540.65 MB for "
                                      "537.46 MB algorithmic; scaled to this workload by algorithmic bytes"}}
 
 
@@ -284,6 +284,23 @@ def store_bytes(T, Hkv=HKV, Dh=D):
 
 # ------------------------------------------------------- headline workload
 
+METRIC = "paged decode-attn HBM GB/s (% of peak) & us/layer; packed prefill TFLOP/s"
+
+
+def headline_config(world):
+    """The headline workload, named the same way by both arms."""
+    return {"workload": "B=1 paged decode step (RoPE + KV store + split-KV decode fused in one launch per layer), "
+                        "Hq=32 Hkv=8 D=128, KV [32 layers, 65536 slots, 8, 128] bf16, page 16, "
+                        "contexts 1K-32K x 32 layers",
+            "contexts": SWEEP, "layers": N_LAYERS, "page_size": PAGE, "max_splits": MAX_SPLITS,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "no flush: 8.5 GB step footprint (32-layer rotation) >> 129 MB L2",
+            "timing": "CUDA events on the launch stream around K replays of the captured step graph",
+            "launch_overlap": "programmatic dependent launch, index arrays read before the wait "
+                              "(pa_set_launch_overlap(PA_OVERLAP_EARLY_METADATA))"}
+
+
+
 class DecodeSweep:
     """The 32-layer B=1 decode sweep, with every input resident on the device."""
 
@@ -436,19 +453,11 @@ def run_ours(args, rank, world, local):
 
     dev_err = api.pa_get_error(sw.ws, stream=s) | api.pa_get_error_word(sw.err, stream=s)
     line = {
-        "metric": "paged decode-attn HBM GB/s (% of peak) & us/layer; packed prefill TFLOP/s",
+        "metric": METRIC,
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, random page permutation)",
-        "config": {"workload": "B=1 paged decode step (RoPE + KV store + split-KV decode fused in one launch per "
-                               "layer), Hq=32 Hkv=8 D=128, "
-                               "KV [32 layers, 65536 slots, 8, 128] bf16, page 16, contexts 1K-32K x 32 layers",
-                   "contexts": SWEEP, "layers": N_LAYERS, "page_size": PAGE, "max_splits": MAX_SPLITS,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "no flush: 8.5 GB step footprint (32-layer rotation) >> 129 MB L2",
-                   "timing": "CUDA events on the launch stream around K replays of the captured step graph",
-                   "launch_overlap": "programmatic dependent launch, index arrays read before the wait "
-                                     "(pa_set_launch_overlap(PA_OVERLAP_EARLY_METADATA))"},
+        "config": headline_config(world),
         "gpu_launches": sw.launches_per_step * args.steps,
         "gpu_launches_per_step": sw.launches_per_step,
         "frac_of_hbm_peak": round(value / peaks["hbm_gbs"], 4),
@@ -650,39 +659,43 @@ def cpu_baseline(sw):
 
 
 def run_reference(args, rank, world, local):
-    """The float64 oracle as the reference arm: each step is one layer-call of
-    the sweep (context cycling 1K..32K), timed on one host core."""
+    """The float64 oracle as the reference arm, on the host cores only: the
+    CUDA library is never loaded and no device memory is used.  Each step is
+    a bounded sample of the headline workload -- one layer-call (RoPE + store
+    + decode) of the sweep, contexts cycling 1K..32K -- over a cache drawn on
+    the host with the sweep's shapes and distribution (one layer)."""
     if rank != 0:
         return None
     import oracle
     oracle.build()
-    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
-    if dev.type == "cuda":
-        torch.cuda.set_device(dev)
-    sw = DecodeSweep(dev)
-    cos, sin = sw.cos.cpu().numpy(), sw.sin.cpu().numpy()
-    prepared = []
-    for p, n in enumerate(SWEEP):
-        prepared.append(_oracle_inputs(sw.kv, 17, n, sw.q[p, 17], sw.k_new[p, 17], sw.v_new[p, 17]))
+    kv = W.make_paged_kv(lens=[SWEEP[-1]], n_layers=1, size=SIZE, n_kv_heads=HKV, head_dim=D, page_size=PAGE,
+                         seed=2, max_ctx=SWEEP[-1], device="cpu")
+    g = W.generator(2 + 104729)
+    P = len(SWEEP)
+    q = W.bf16_normal((P, 1, HQ, D), g)
+    k_new = W.bf16_normal((P, 1, HKV, D), g)
+    v_new = W.bf16_normal((P, 1, HKV, D), g)
+    cos, sin = (t.numpy() for t in W.rope_tables(W.ROPE_MAX_POS, D))
+    scale = 1.0 / math.sqrt(D)
+    prepared = [_oracle_inputs(kv, 0, n, q[p], k_new[p], v_new[p]) for p, n in enumerate(SWEEP)]
     for i in range(args.warmup):
-        p = i % len(SWEEP)
-        _oracle_layer_call(oracle, *prepared[p], SWEEP[p], cos, sin, sw.scale)
+        p = i % P
+        _oracle_layer_call(oracle, *prepared[p], SWEEP[p], cos, sin, scale)
     t_tot, b_tot = 0.0, 0
     for i in range(args.steps):
-        p = i % len(SWEEP)
+        p = i % P
         t0 = time.perf_counter()
-        _oracle_layer_call(oracle, *prepared[p], SWEEP[p], cos, sin, sw.scale)
+        _oracle_layer_call(oracle, *prepared[p], SWEEP[p], cos, sin, scale)
         t_tot += time.perf_counter() - t0
         b_tot += decode_bytes(SWEEP[p]) + rope_bytes(1) + store_bytes(1)
     val = b_tot / t_tot / 1e9
-    return {"metric": "paged decode-attn HBM GB/s (% of peak) & us/layer; packed prefill TFLOP/s",
-            "value": round(val, 4), "unit": "GB/s", "impl": "reference", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(t_tot / args.steps * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "B=1 paged decode layer-call (RoPE + KV store + decode), Hq=32 Hkv=8 D=128, "
-                                   "page 16, contexts cycling 1K-32K (one layer-call per step)"},
-            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": "one layer-call per step, contexts cycling 1K..32K"},
+    sample = (f"one layer-call per step (RoPE + KV store + decode), contexts cycling 1K..32K, {args.steps} steps, "
+              f"{t_tot:.1f} s single-threaded float64 C; host has {os.cpu_count()} cores")
+    return {"metric": METRIC, "value": round(val, 4), "unit": "GB/s", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_tot / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": headline_config(world),
+            "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -132,7 +132,10 @@ pa_status pa_workspace_init(void *workspace, size_t workspace_bytes, cudaStream_
 /* Copy the workspace's device error word to *device_error.  Synchronises `st`
  * (keep it out of the hot loop and out of graph capture).  Returns
  * PA_ERR_DEVICE_INDEX if the word is non-zero, PA_OK otherwise.  The word is
- * sticky: pa_workspace_init clears it. */
+ * sticky: pa_workspace_init clears it.  After PA_DEVERR_TIMEOUT the aborted
+ * call may have left decode merge counters non-zero: call pa_workspace_init
+ * before the workspace is used again (index-error bits alone leave the
+ * counters intact). */
 pa_status pa_get_error(const void *workspace, int32_t *device_error, cudaStream_t st);
 
 /* Same, for a bare int32 error word passed to pa_kv_store / pa_rope_packed. */
@@ -210,7 +213,10 @@ pa_status pa_paged_decode_attn(const void *q, int batch, int n_q_heads, const vo
  *   - Size limit: the partials of `batch` requests must fit the 16 MiB:
  *     16 MiB >= 1024 + batch * (n_kv_heads*4 + max_splits*n_q_heads*(head_dim+2)*4)
  *     (e.g. 15 requests at Hq=32, head_dim 128, max_splits 64); larger calls
- *     return PA_ERR_WORKSPACE and enqueue nothing.
+ *     return PA_ERR_WORKSPACE.
+ *   - Every argument check (those of pa_paged_decode_attn, the size limit,
+ *     error_word's alignment) runs before the first CUDA call: a call that
+ *     returns an error has enqueued nothing and written nothing.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.

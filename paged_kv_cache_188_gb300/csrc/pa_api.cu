@@ -2,6 +2,9 @@
 // initialisation, device error word readback.
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <vector>
+
 #include "pa_internal.h"
 
 namespace pa {
@@ -20,6 +23,32 @@ int num_sms()
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (dev >= 0 && dev < 64) cached[dev] = n;
     return n;
+}
+
+bool ensure_dynamic_smem(const void *kern, size_t bytes)
+{
+    struct Rec {
+        const void *kern;
+        int dev;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Rec> recs;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (Rec &r : recs) {
+        if (r.kern != kern || r.dev != dev) continue;
+        if (r.bytes >= bytes) return true;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+            return false;
+        r.bytes = bytes;
+        return true;
+    }
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return false;
+    recs.push_back(Rec{kern, dev, bytes});
+    return true;
 }
 
 static size_t per_request_bytes(int n_q_heads, int n_kv_heads, int head_dim, int max_splits)

@@ -55,9 +55,11 @@ extern "C" pa_status pa_paged_decode_attn_noalloc(const void *q, int batch, int 
                                                   cudaStream_t st)
 {
     using namespace pa;
-    if (n_q_heads <= 0 || s.n_kv_heads <= 0 || s.head_dim <= 0 || max_splits < 1 || max_splits > kDecMaxSplits ||
-        batch < 0)
-        return PA_ERR_SHAPE;
+    // every check runs before the first CUDA call: a call that fails has
+    // enqueued nothing and written nothing
+    const pa_status rc0 = check_decode_args(q, batch, n_q_heads, k_buf, v_buf, s, layer_id, req_to_token, req_rows,
+                                            max_ctx, req_pool_indices, seq_lens, max_splits, out);
+    if (rc0 != PA_OK) return rc0;
     const DecodeWsLayout ws = decode_ws_layout(kNoAllocScratchBytes, n_q_heads, s.n_kv_heads, s.head_dim, max_splits);
     if (ws.cap_batch < batch || ws.total > kNoAllocScratchBytes) return PA_ERR_WORKSPACE;   // beyond the fixed array
     if (error_word && !aligned4(error_word)) return PA_ERR_ALIGN;

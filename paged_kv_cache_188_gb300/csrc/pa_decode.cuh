@@ -1129,12 +1129,7 @@ static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
     auto kern = paged_decode_kernel<D, S, NH, MODE>;
     const size_t smem = DecSmem<D, S, NH, MODE == MODE_FP8>::bytes(a.batch);
     if (smem > kSmemLimit) return PA_ERR_UNSUPPORTED;
-    static size_t configured = 0;
-    if (smem > configured) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return PA_ERR_CUDA;
-        configured = smem;
-    }
+    if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kern), smem)) return PA_ERR_CUDA;
     if (launch_kernel(kern, dim3(num_sms()), dim3(kDecThreads), smem, st, a) != cudaSuccess) return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -1167,11 +1162,13 @@ struct StepInputs {
     int max_pos;
 };
 
-// Validation shared by every entry point (argument ranges, alignment).
-static pa_status check_decode(const void *q, int batch, int n_q_heads, const void *k_buf, const void *v_buf,
-                              pa_kv_shape s, int layer_id, const int32_t *req_to_token, int req_rows, int max_ctx,
-                              const int32_t *req_pool_indices, const int32_t *seq_lens, void *workspace,
-                              int max_splits, void *out)
+// Validation of the arguments every decode entry point shares (ranges,
+// supported shapes, null pointers, alignment); the workspace is checked by
+// the caller of this function.  Touches no CUDA state.
+static pa_status check_decode_args(const void *q, int batch, int n_q_heads, const void *k_buf, const void *v_buf,
+                                   pa_kv_shape s, int layer_id, const int32_t *req_to_token, int req_rows,
+                                   int max_ctx, const int32_t *req_pool_indices, const int32_t *seq_lens,
+                                   int max_splits, void *out)
 {
     if (batch < 0 || batch > kDecMaxBatch || n_q_heads <= 0 || s.n_layers <= 0 || s.size <= 0 ||
         s.n_kv_heads <= 0 || req_rows <= 0 || max_ctx <= 0 || max_splits < 1 || max_splits > kDecMaxSplits)
@@ -1181,14 +1178,28 @@ static pa_status check_decode(const void *q, int batch, int n_q_heads, const voi
     const int G = n_q_heads / s.n_kv_heads;
     if (G > 16 || (s.head_dim != 64 && s.head_dim != 128)) return PA_ERR_UNSUPPORTED;
     if ((int64_t)s.n_layers * s.size >= (int64_t)INT32_MAX - 16) return PA_ERR_SHAPE;
-    if (!workspace) return PA_ERR_NULL;
-    if (!aligned256(workspace)) return PA_ERR_ALIGN;
     if (batch == 0) return PA_OK;
     if (!q || !k_buf || !v_buf || !req_to_token || !req_pool_indices || !seq_lens || !out) return PA_ERR_NULL;
     if (!aligned16(q) || !aligned16(k_buf) || !aligned16(v_buf) || !aligned16(out) || !aligned4(req_to_token) ||
         !aligned4(req_pool_indices) || !aligned4(seq_lens))
         return PA_ERR_ALIGN;
     return PA_OK;
+}
+
+// Validation shared by the workspace entry points: the arguments, then the
+// workspace pointer.
+static pa_status check_decode(const void *q, int batch, int n_q_heads, const void *k_buf, const void *v_buf,
+                              pa_kv_shape s, int layer_id, const int32_t *req_to_token, int req_rows, int max_ctx,
+                              const int32_t *req_pool_indices, const int32_t *seq_lens, void *workspace,
+                              int max_splits, void *out)
+{
+    // the workspace checks come first for an empty batch, as before
+    const pa_status rc = check_decode_args(q, batch, n_q_heads, k_buf, v_buf, s, layer_id, req_to_token, req_rows,
+                                           max_ctx, req_pool_indices, seq_lens, max_splits, out);
+    if (rc != PA_OK && rc != PA_ERR_NULL && rc != PA_ERR_ALIGN) return rc;
+    if (!workspace) return PA_ERR_NULL;
+    if (!aligned256(workspace)) return PA_ERR_ALIGN;
+    return rc;
 }
 
 // Launch arguments for `batch` requests of `n_q_heads` heads whose split

@@ -25,6 +25,12 @@ inline bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) &
 // SM count of the current device (cached per device; a property, not call state).
 int num_sms();
 
+// Raise the dynamic shared-memory limit of kernel `kern` on the current device
+// to at least `bytes`.  The attribute is per device, so the largest value set
+// is remembered per (kernel, device), under a lock.  false if the runtime
+// refused.
+bool ensure_dynamic_smem(const void *kern, size_t bytes);
+
 // Current launch-overlap mode (PA_OVERLAP_*).
 int launch_overlap();
 

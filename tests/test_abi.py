@@ -213,3 +213,27 @@ def test_fp8_wrappers_reject_wrong_cache_dtypes_before_the_library():
     u8 = torch.zeros((1, 4, 1, 64), dtype=torch.uint8)
     with pytest.raises(TypeError, match="CUDA tensor"):            # host memory is never passed down
         api.pa_kv_store_fp8(u8, u8, 0, None, None, None, sc, sc)
+
+
+def test_noalloc_validation_runs_before_any_cuda_call(lib):
+    # On a machine without a GPU, a call that got past validation would fail
+    # in the CUDA runtime (PA_ERR_CUDA); each of these must instead return its
+    # validation error, so nothing was enqueued or written.
+    P = ctypes.c_void_p
+
+    def call(**kw):
+        a = dict(q=FAKE, batch=1, hq=8, s=_shape(), layer=0, splits=4, out=FAKE, err=None)
+        a.update(kw)
+        return lib.pa_paged_decode_attn_noalloc(P(a["q"]), a["batch"], a["hq"], P(FAKE), P(FAKE), a["s"], a["layer"],
+                                                P(FAKE), 1, 16, P(FAKE), P(FAKE), 0.125, a["splits"], P(a["out"]),
+                                                P(a["err"]) if a["err"] else None, None)
+    assert call(q=0) == 1                         # null q
+    assert call(out=FAKE + 8) == 3
+    assert call(s=_shape(d=96)) == 4              # unsupported head_dim
+    assert call(hq=64) == 4                       # G = 32 > 16
+    assert call(hq=7) == 2
+    assert call(layer=2) == 2
+    assert call(splits=129) == 2
+    assert call(batch=4000, hq=32, s=_shape(hkv=8, d=128), splits=64) == 5   # beyond the 16 MiB array
+    assert call(err=FAKE + 2) == 3
+    assert call(batch=0, q=0, out=0) == 0

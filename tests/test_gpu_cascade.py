@@ -23,15 +23,20 @@ def _lib():
 
 
 def _case(lens, hq, hkv, group_size, prefix, seed, d=128, size=65536):
+    """The step's inputs, its new K/V stored on the device by the library, and
+    the expected cache built on the host by the oracle's store from the same
+    inputs (the oracle never sees a value the library wrote)."""
     st = W.make_decode_step(lens=lens, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, n_layers=1, size=size,
                             page_size=16, seed=seed, max_ctx=max(lens) + 16, shared_prefix=(group_size, prefix),
                             device="cuda")
+    kb0, vb0 = bits(st.kv.k_buf), bits(st.kv.v_buf)
     api.pa_kv_store(st.kv.k_buf, st.kv.v_buf, st.layer, st.k_new, st.v_new, st.loc)
-    return st
+    kb, vb = oracle.kv_store(kb0, vb0, st.layer, bits(st.k_new), bits(st.v_new), npy(st.loc))
+    return st, kb, vb
 
 
-def _ref(st):
-    return oracle.decode(bits(st.q), bits(st.kv.k_buf), bits(st.kv.v_buf), st.layer, npy(st.kv.req_to_token),
+def _ref(st, kb, vb):
+    return oracle.decode(bits(st.q), kb, vb, st.layer, npy(st.kv.req_to_token),
                          npy(st.kv.req_pool_indices), npy(st.kv.seq_lens), st.scale)
 
 
@@ -51,21 +56,21 @@ def test_cascade_matches_oracle(hq, hkv):
     # groups of 5 (chunks of 16/G members leave partial chunks), ragged lengths,
     # one member shorter than the prefix window
     lens = [3000, 1500, 700, 2500, 130, 4000, 1100, 900, 2048, 5000, 64]
-    st = _case(lens, hq, hkv, 5, 512, seed=hq + hkv)
+    st, kb, vb = _case(lens, hq, hkv, 5, 512, seed=hq + hkv)
     indptr, reqs, prefix = W.prefix_groups(lens, 5, 512, 16)
     caps = (len(lens), 3, 5, MAX_SPLITS)
     out, ws = _cascade(st, indptr, reqs, prefix, caps)
     assert api.pa_get_error(ws) == 0
-    assert_attention_close(npy(out.float()), _ref(st), f"cascade hq={hq} hkv={hkv}")
+    assert_attention_close(npy(out.float()), _ref(st, kb, vb), f"cascade hq={hq} hkv={hkv}")
 
 
 def test_cascade_config3_shape_and_repeat_calls():
     lens = W.cfg_lens_uniform(32, 512, 8192, seed=3)
-    st = _case(lens, 32, 8, 8, 1024, seed=3, size=262144)
+    st, kb, vb = _case(lens, 32, 8, 8, 1024, seed=3, size=262144)
     indptr, reqs, prefix = W.prefix_groups(lens, 8, 1024, 16)
     caps = (32, 4, 8, MAX_SPLITS)
     out, ws = _cascade(st, indptr, reqs, prefix, caps)
-    ref = _ref(st)
+    ref = _ref(st, kb, vb)
     assert_attention_close(npy(out.float()), ref, "cascade config-3 shape")
     # a second call on the same workspace (tickets back at zero), then groups
     # that leave requests out: the results stay within tolerance

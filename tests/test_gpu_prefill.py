@@ -156,19 +156,27 @@ def test_last_rows_gathered_by_the_epilogue():
     new, pre = [1, 31, 200, 64, 129], [0, 40, 300, 0, 17]
     pb = W.make_prefill_batch(new_lens=new, prefix_lens=pre, n_q_heads=32, n_kv_heads=8, head_dim=128, size=8192,
                               page_size=16, seed=21, device="cuda")
-    _store(pb)
+    kb, vb = _store(pb)
     ws = api.alloc_workspace(api.pa_prefill_workspace_bytes())
     R = len(new)
     out = torch.full_like(pb.q, float("nan"))
     last = torch.full((R,) + tuple(pb.q.shape[1:]), float("nan"), dtype=torch.bfloat16, device="cuda")
     api.pa_paged_prefill_attn(pb.q, pb.kv.k_buf, pb.kv.v_buf, 0, pb.qo_indptr, pb.kv_indptr, pb.kv.req_to_token,
                               pb.kv.req_pool_indices, pb.scale, ws, out, last_out=last)
-    ref, _ = _run(pb)
     torch.cuda.synchronize()
-    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))    # the gather changes nothing else
-    rows = (pb.qo_indptr[1:] - 1).long()
-    assert torch.equal(last.view(torch.int16), ref[rows].view(torch.int16))
     assert api.pa_get_error(ws) == 0
+    # each request's last row against the oracle, every head, from the
+    # host-built cache
+    Hq = pb.q.shape[1]
+    last_rows = npy(pb.qo_indptr)[1:] - 1
+    sel = (np.repeat(last_rows.astype(np.int32), Hq), np.tile(np.arange(Hq, dtype=np.int32), R))
+    ref_last = _ref(pb, kb, vb, sel=sel).reshape(R, Hq, -1)
+    assert_attention_close(npy(last.float()), ref_last, "last rows gathered by the epilogue")
+    # the gather is a copy of those rows of out, and changes nothing else
+    plain, _ = _run(pb)
+    assert torch.equal(out.view(torch.int16), plain.view(torch.int16))
+    rows = (pb.qo_indptr[1:] - 1).long()
+    assert torch.equal(last.view(torch.int16), out[rows].view(torch.int16))
 
 
 @pytest.mark.parametrize("G", [1, 4, 16])
