@@ -74,6 +74,9 @@ def _load():
         lib.ora_decode_fp8.argtypes = [P, i32, i32, P, P, i32, i64, i32, i32, i32,
                                        P, i32, i32, P, P, dbl, P, P, P, P, i64, P]
         lib.ora_decode_fp8.restype = i32
+        lib.ora_prefill_fp8.argtypes = [P, i64, i32, P, P, i32, i64, i32, i32, i32,
+                                        P, P, i32, P, i32, i32, P, dbl, P, P, P, P, i64, P]
+        lib.ora_prefill_fp8.restype = i32
         _lib = lib
     return _lib
 
@@ -267,4 +270,39 @@ def decode_fp8(q_bits, k_buf, v_buf, layer, req_to_token, req_pool_indices, seq_
                                 rp, r2t.shape[0], r2t.shape[1], rpip, slp, float(scale), ksp, vsp,
                                 sb, sh, nsel, out.ctypes.data_as(ctypes.c_void_p))
     _check(rc, "decode_fp8")
+    return out
+
+
+def prefill_fp8(q_bits, k_buf, v_buf, layer, qo_indptr, kv_indptr, req_to_token, req_pool_indices, scale,
+                k_scale, v_scale, sel=None):
+    """Ragged causal prefill in float64 over an e4m3 cache with per-(layer, kv
+    head) scales.  Same shapes and ``sel`` as ``prefill``; see
+    ``ora_prefill_fp8``."""
+    q, qp = _c(q_bits, np.uint16)
+    T, Hq, D = q.shape
+    kb, kp = _c(k_buf, np.uint8)
+    vb, vp = _c(v_buf, np.uint8)
+    n_layers, size, Hkv, D2 = kb.shape
+    assert D2 == D and vb.shape == kb.shape
+    ks, ksp = _c(k_scale, np.float32)
+    vs, vsp = _c(v_scale, np.float32)
+    assert ks.shape == (n_layers, Hkv) and vs.shape == (n_layers, Hkv)
+    qo, qop = _c(qo_indptr, np.int32)
+    kv, kvp = _c(kv_indptr, np.int32)
+    R = qo.size - 1
+    r2t, rp = _c(req_to_token, np.int32)
+    rpi, rpip = _c(req_pool_indices, np.int32)
+    if sel is None:
+        out = np.empty((T, Hq, D), dtype=np.float64)
+        st = sh = None
+        nsel = 0
+    else:
+        stt, st = _c(sel[0], np.int32)
+        shh, sh = _c(sel[1], np.int32)
+        nsel = stt.size
+        out = np.empty((nsel, D), dtype=np.float64)
+    rc = _load().ora_prefill_fp8(qp, T, Hq, kp, vp, n_layers, size, Hkv, D, layer, qop, kvp, R,
+                                 rp, r2t.shape[0], r2t.shape[1], rpip, float(scale), ksp, vsp,
+                                 st, sh, nsel, out.ctypes.data_as(ctypes.c_void_p))
+    _check(rc, "prefill_fp8")
     return out

@@ -498,3 +498,90 @@ int ora_decode_fp8(const uint16_t *q, int B, int Hq, const uint8_t *k_buf,
     free(scores);
     return ORA_OK;
 }
+
+/* Ragged causal prefill over an fp8 cache: as ora_prefill (same request
+ * layout, bottom-right aligned causal mask, selection and checks), with key j
+ * of kv head h read as e4m3_value(K8[slot_j, h, :]) * k_scale[layer, h] and
+ * value rows likewise with v_scale.  The scheme is the reading stated above
+ * ora_kv_store_fp8 (page "e58a728" names only an fp8 test). */
+int ora_prefill_fp8(const uint16_t *q, int64_t T, int Hq, const uint8_t *k_buf,
+                    const uint8_t *v_buf, int n_layers, int64_t size, int Hkv,
+                    int D, int layer, const int32_t *qo_indptr,
+                    const int32_t *kv_indptr, int R, const int32_t *req_to_token,
+                    int req_rows, int max_ctx, const int32_t *req_pool_indices,
+                    double scale, const float *k_scale, const float *v_scale,
+                    const int32_t *sel_t, const int32_t *sel_h, int64_t n_sel,
+                    double *out)
+{
+    if (Hkv <= 0 || Hq % Hkv != 0 || layer < 0 || layer >= n_layers || D <= 0 || R < 0)
+        return ORA_ERR_SHAPE;
+    if (qo_indptr[0] != 0 || qo_indptr[R] != T || kv_indptr[0] != 0)
+        return ORA_ERR_SHAPE;
+    for (int r = 0; r < R; ++r) {
+        int n_r = qo_indptr[r + 1] - qo_indptr[r];
+        int L_r = kv_indptr[r + 1] - kv_indptr[r];
+        if (n_r < 0 || L_r < n_r || L_r > max_ctx)
+            return ORA_ERR_SHAPE;
+        int row = req_pool_indices[r];
+        if (row < 0 || row >= req_rows)
+            return ORA_ERR_INDEX;
+        for (int j = 0; j < L_r; ++j) {
+            int32_t s = req_to_token[(int64_t)row * max_ctx + j];
+            if (s < 0 || (int64_t)s >= size)
+                return ORA_ERR_INDEX;
+        }
+    }
+    const int G = Hq / Hkv;
+    const int64_t slot_stride = (int64_t)Hkv * D;
+    double *scores = (double *)malloc(sizeof(double) * (size_t)(max_ctx > 0 ? max_ctx : 1));
+    if (!scores)
+        return ORA_ERR_NOMEM;
+    const int64_t npairs = sel_t ? n_sel : T * Hq;
+    for (int64_t i = 0; i < npairs; ++i) {
+        int64_t t = sel_t ? sel_t[i] : i / Hq;
+        int hq = sel_t ? sel_h[i] : (int)(i % Hq);
+        if (t < 0 || t >= T || hq < 0 || hq >= Hq) {
+            free(scores);
+            return ORA_ERR_SHAPE;
+        }
+        int r = 0;
+        while (!(qo_indptr[r] <= t && t < qo_indptr[r + 1]))
+            ++r;
+        int n_r = qo_indptr[r + 1] - qo_indptr[r];
+        int L_r = kv_indptr[r + 1] - kv_indptr[r];
+        int64_t n = (L_r - n_r) + (t - qo_indptr[r]) + 1;   /* positions 0 .. p_r + i */
+        int h = hq / G;
+        const int32_t *slots = req_to_token + (int64_t)req_pool_indices[r] * max_ctx;
+        const uint16_t *qv = q + (t * Hq + hq) * D;
+        const uint8_t *k0 = k_buf + (int64_t)layer * size * slot_stride + (int64_t)h * D;
+        const uint8_t *v0 = v_buf + (int64_t)layer * size * slot_stride + (int64_t)h * D;
+        const double ks = (double)k_scale[(int64_t)layer * Hkv + h];
+        const double vs = (double)v_scale[(int64_t)layer * Hkv + h];
+        double *o = out + i * D;
+        for (int d = 0; d < D; ++d)
+            o[d] = 0.0;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < n; ++j) {
+            const uint8_t *kr = k0 + (int64_t)slots[j] * slot_stride;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+                dot += ora_bf16_to_f64(qv[d]) * (ora_e4m3_to_f64(kr[d]) * ks);
+            scores[j] = scale * dot;
+            if (scores[j] > m)
+                m = scores[j];
+        }
+        double denom = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            scores[j] = exp(scores[j] - m);
+            denom += scores[j];
+        }
+        for (int64_t j = 0; j < n; ++j) {
+            const uint8_t *vr = v0 + (int64_t)slots[j] * slot_stride;
+            double w = scores[j] / denom;
+            for (int d = 0; d < D; ++d)
+                o[d] += w * (ora_e4m3_to_f64(vr[d]) * vs);
+        }
+    }
+    free(scores);
+    return ORA_OK;
+}

@@ -508,3 +508,72 @@ def test_decode_fp8_with_power_of_two_scales_equals_bf16_decode():
     ref = oracle.decode(bits(st.q), kbf, vbf, 1, *args)
     out = oracle.decode_fp8(bits(st.q), k8, v8, 1, *args, ks, vs)
     np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-15)
+
+
+def _fp8_prefill(new, pre, Hq, Hkv, D, page, seed, ks=None, vs=None):
+    """A prefill batch over an fp8 cache: the complete bf16 cache (prefix +
+    new tokens, stored by the oracle) quantised with per-(layer, kv head)
+    scales by the oracle's encoder."""
+    pb = W.make_prefill_batch(new_lens=new, prefix_lens=pre, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D,
+                              size=256, page_size=page, seed=seed, req_rows=len(new) + 2)
+    kb, vb = _prefill_complete(pb)
+    rng = np.random.default_rng(seed)
+    L = kb.shape[0]
+    ks = (rng.uniform(0.5, 2.0, (L, Hkv)) / 112).astype(np.float32) if ks is None else ks
+    vs = (rng.uniform(0.5, 2.0, (L, Hkv)) / 112).astype(np.float32) if vs is None else vs
+    k8 = oracle.f32_to_e4m3(oracle.bf16_to_f64(kb).astype(np.float32) / ks[:, None, :, None])
+    v8 = oracle.f32_to_e4m3(oracle.bf16_to_f64(vb).astype(np.float32) / vs[:, None, :, None])
+    return pb, k8, v8, ks, vs
+
+
+def _prefill_fp8_args(pb):
+    return (pb.qo_indptr.numpy(), pb.kv_indptr.numpy(), pb.kv.req_to_token.numpy(),
+            pb.kv.req_pool_indices.numpy(), pb.scale)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,page", [(6, 3, 8, 4), (8, 2, 16, 1), (4, 4, 32, 16)])
+def test_prefill_fp8_matches_masked_library_attention_on_dequantised_cache(Hq, Hkv, D, page):
+    new, pre = [5, 17, 1, 9], [11, 0, 6, 32]
+    pb, k8, v8, ks, vs = _fp8_prefill(new, pre, Hq, Hkv, D, page, seed=61 + D)
+    out = oracle.prefill_fp8(bits(pb.q), k8, v8, pb.layer, *_prefill_fp8_args(pb), ks, vs)
+    kf = _torch_e4m3_values(k8) * ks[:, None, :, None].astype(np.float64)
+    vf = _torch_e4m3_values(v8) * vs[:, None, :, None].astype(np.float64)
+    qf = oracle.bf16_to_f64(bits(pb.q))
+    G = Hq // Hkv
+    t0 = 0
+    for r, (n, p) in enumerate(zip(new, pre)):
+        row = int(pb.kv.req_pool_indices[r])
+        slots = pb.kv.req_to_token[row, :p + n].numpy()
+        mask = np.arange(p + n)[None, :] <= (p + np.arange(n))[:, None]   # bottom-right aligned
+        for hq in range(Hq):
+            ref = _sdpa_f64(qf[t0:t0 + n, hq], kf[pb.layer, slots, hq // G], vf[pb.layer, slots, hq // G],
+                            pb.scale, mask=mask)
+            np.testing.assert_allclose(out[t0:t0 + n, hq], ref, rtol=1e-12, atol=1e-12)
+        t0 += n
+
+
+def test_prefill_fp8_with_power_of_two_scales_equals_bf16_prefill():
+    # e4m3 values times 2^k are bf16 numbers: the bf16 oracle on that cache
+    # computes the same attention in the same order
+    ks = np.array([[2.0 ** -5, 2.0 ** -7]], np.float32)
+    vs = np.array([[2.0 ** -3, 1.0]], np.float32)
+    pb, k8, v8, _, _ = _fp8_prefill([7, 3, 12], [4, 20, 0], 8, 2, 16, 4, seed=63, ks=ks, vs=vs)
+    kbf = oracle.f64_to_bf16(oracle.e4m3_to_f64(k8) * ks[:, None, :, None])
+    vbf = oracle.f64_to_bf16(oracle.e4m3_to_f64(v8) * vs[:, None, :, None])
+    ref = oracle.prefill(bits(pb.q), kbf, vbf, pb.layer, *_prefill_fp8_args(pb))
+    out = oracle.prefill_fp8(bits(pb.q), k8, v8, pb.layer, *_prefill_fp8_args(pb), ks, vs)
+    np.testing.assert_array_equal(out, ref)
+
+
+def test_prefill_fp8_last_row_equals_fp8_decode_and_selection_matches():
+    new, pre = [7, 3, 12], [4, 20, 0]
+    pb, k8, v8, ks, vs = _fp8_prefill(new, pre, 4, 1, 8, 4, seed=64)
+    out = oracle.prefill_fp8(bits(pb.q), k8, v8, pb.layer, *_prefill_fp8_args(pb), ks, vs)
+    last = pb.qo_indptr.numpy()[1:] - 1
+    dec = oracle.decode_fp8(bits(pb.q)[last], k8, v8, pb.layer, pb.kv.req_to_token.numpy(),
+                            pb.kv.req_pool_indices.numpy(), np.array([p + n for p, n in zip(pre, new)], np.int32),
+                            pb.scale, ks, vs)
+    np.testing.assert_array_equal(out[last], dec)
+    sel = oracle.prefill_fp8(bits(pb.q), k8, v8, pb.layer, *_prefill_fp8_args(pb), ks, vs,
+                             sel=(np.array([21, 0, 9], np.int32), np.array([3, 0, 2], np.int32)))
+    np.testing.assert_array_equal(sel, out[[21, 0, 9], [3, 0, 2]])
