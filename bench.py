@@ -71,7 +71,7 @@ def parse():
     p.add_argument("--only-main", action="store_true", help="skip the secondary workloads")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--no-fp8", action="store_true", help="skip the sweep over an e4m3 copy of the cache")
-    p.add_argument("--profile", choices=["decode", "prefill", "rope", "store"], default=None,
+    p.add_argument("--profile", choices=["decode", "prefill", "prefill_fp8", "rope", "store"], default=None,
                    help="run a small fixed case of one kernel (for ncu captures) and exit")
     return p.parse_args()
 
@@ -296,8 +296,8 @@ def headline_config(world):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": "no flush: 8.5 GB step footprint (32-layer rotation) >> 129 MB L2",
             "timing": "CUDA events on the launch stream around K replays of the captured step graph",
-            "launch_overlap": "programmatic dependent launch, index arrays read before the wait "
-                              "(pa_set_launch_overlap(PA_OVERLAP_EARLY_METADATA))"}
+            "launch_overlap": "programmatic dependent launch; index arrays and K/V rows other than each "
+                              "request's newest read before the wait (pa_set_launch_overlap(PA_OVERLAP_EARLY_KV))"}
 
 
 
@@ -367,9 +367,11 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
     # the step's index arrays (seq_lens, req_to_token, positions, loc) never
-    # change inside a step, so kernels may read them before the preceding
-    # kernel ends (programmatic dependent launch, early-metadata mode)
-    api.pa_set_launch_overlap(api.OVERLAP_EARLY_METADATA)
+    # change inside a step, and no kernel writes a cache row other than a
+    # request's newest, so kernels may read the index arrays and the older
+    # K/V rows before the preceding kernel ends (programmatic dependent
+    # launch, early-KV mode)
+    api.pa_set_launch_overlap(api.OVERLAP_EARLY_KV)
     sw = DecodeSweep(dev)
     s = sw.stream
     torch.cuda.set_stream(s)   # graph replays, events and copies all go to the launch stream
@@ -501,6 +503,8 @@ def secondary_workloads(dev, peaks, s):
     def prefill():
         api.pa_paged_prefill_attn(pb.q, pb.kv.k_buf, pb.kv.v_buf, 0, pb.qo_indptr, pb.kv_indptr,
                                   pb.kv.req_to_token, pb.kv.req_pool_indices, pb.scale, ws, out, stream=s)
+    # the new tokens' K/V are in the cache before attention reads them
+    api.pa_kv_store(pb.kv.k_buf, pb.kv.v_buf, 0, pb.k_new, pb.v_new, pb.loc, stream=s)
     try:
         prefill()
         torch.cuda.synchronize()
@@ -525,6 +529,47 @@ def secondary_workloads(dev, peaks, s):
                                              "tflops": round(dflops / (ms * 1e-3) / 1e12, 1)}
     except api.PaError as e:
         res["prefill"]["dense_no_prefix"] = {"unavailable": str(e)}
+    # the same prompts over an e4m3 copy of the cache (one scale per kv head)
+    try:
+        n_layers, size = pb.kv.k_buf.shape[0], pb.kv.k_buf.shape[1]
+        k8 = torch.empty((n_layers, size, HKV, D), dtype=torch.uint8, device=dev)
+        v8 = torch.empty_like(k8)
+        ks = torch.full((n_layers, HKV), 4.5 / 448, dtype=torch.float32, device=dev)
+        vs = ks.clone()
+        every = torch.arange(size, dtype=torch.int32, device=dev)
+        api.pa_kv_store_fp8(k8, v8, 0, pb.kv.k_buf[0], pb.kv.v_buf[0], every, ks, vs, stream=s)
+        fp8 = lambda: api.pa_paged_prefill_attn_fp8(pb.q, k8, v8, 0, pb.qo_indptr, pb.kv_indptr,  # noqa: E731
+                                                    pb.kv.req_to_token, pb.kv.req_pool_indices, pb.scale, ks, vs,
+                                                    ws, out, stream=s)
+        fp8()
+        torch.cuda.synchronize()
+        g = capture(fp8, s)
+        ms = time_graph(g, 20, s)
+        tf8 = flops / (ms * 1e-3) / 1e12
+        res["prefill"]["fp8_cache"] = {"workload": "the same prompts over an e4m3 KV cache with per-kv-head scales "
+                                                   "(tiles widened to bf16 in shared memory)",
+                                       "ms": round(ms, 4), "tflops": round(tf8, 1),
+                                       "frac_of_bf16_peak": round(tf8 / peaks["bf16_tflops"], 4)}
+        del k8, v8, g
+    except api.PaError as e:
+        res["prefill"]["fp8_cache"] = {"unavailable": str(e)}
+    # the same prompts with token-granular pages (page size 1: row gathers)
+    try:
+        p1 = W.make_prefill_batch(new_lens=pb.new_lens, prefix_lens=pb.prefix_lens, n_q_heads=HQ, n_kv_heads=HKV,
+                                  head_dim=D, size=65536, page_size=1, seed=4, max_ctx=4096, device=dev)
+        api.pa_kv_store(p1.kv.k_buf, p1.kv.v_buf, 0, p1.k_new, p1.v_new, p1.loc, stream=s)
+        out1 = torch.empty_like(p1.q)
+        pf1 = lambda: api.pa_paged_prefill_attn(p1.q, p1.kv.k_buf, p1.kv.v_buf, 0, p1.qo_indptr,  # noqa: E731
+                                                p1.kv_indptr, p1.kv.req_to_token, p1.kv.req_pool_indices,
+                                                p1.scale, ws, out1, stream=s)
+        pf1()
+        torch.cuda.synchronize()
+        g = capture(pf1, s)
+        ms = time_graph(g, 20, s)
+        res["prefill"]["page1"] = {"ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1)}
+        del p1, out1, g
+    except api.PaError as e:
+        res["prefill"]["page1"] = {"unavailable": str(e)}
     g_rope = capture(lambda: api.pa_rope_packed(pb.q, pb.k_new, pb.positions, pb.cos_tab, pb.sin_tab,
                                                 stream=s), s)
     ms = time_graph(g_rope, 20, s)
@@ -729,6 +774,23 @@ def run_profile_case(args):
         torch.cuda.synchronize()
         flops = 4.0 * D * HQ * sum(n * p + n * (n + 1) / 2 for n, p in zip(pb.new_lens, pb.prefix_lens))
         print(json.dumps({"profile": "prefill", "launches": 3, "causal_flops_per_launch": flops,
+                          "device_error_word": api.pa_get_error(ws)}))
+    elif args.profile == "prefill_fp8":
+        pb = W.config4(device=dev)
+        ws = api.alloc_workspace(api.pa_prefill_workspace_bytes(), dev)
+        out = torch.empty_like(pb.q)
+        api.pa_kv_store(pb.kv.k_buf, pb.kv.v_buf, 0, pb.k_new, pb.v_new, pb.loc)
+        k8 = torch.empty(pb.kv.k_buf.shape, dtype=torch.uint8, device=dev)
+        v8 = torch.empty_like(k8)
+        ks = torch.full((1, HKV), 4.5 / 448, dtype=torch.float32, device=dev)
+        every = torch.arange(k8.shape[1], dtype=torch.int32, device=dev)
+        api.pa_kv_store_fp8(k8, v8, 0, pb.kv.k_buf[0], pb.kv.v_buf[0], every, ks, ks)
+        for _ in range(3):
+            api.pa_paged_prefill_attn_fp8(pb.q, k8, v8, 0, pb.qo_indptr, pb.kv_indptr, pb.kv.req_to_token,
+                                          pb.kv.req_pool_indices, pb.scale, ks, ks, ws, out, stream=s)
+        torch.cuda.synchronize()
+        flops = 4.0 * D * HQ * sum(n * p + n * (n + 1) / 2 for n, p in zip(pb.new_lens, pb.prefix_lens))
+        print(json.dumps({"profile": "prefill_fp8", "launches": 3, "causal_flops_per_launch": flops,
                           "device_error_word": api.pa_get_error(ws)}))
     else:
         pb = W.config4(device=dev)

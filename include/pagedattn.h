@@ -92,13 +92,37 @@ const char *pa_status_string(pa_status s);
  *     first page-table entries are ready when the earlier kernel ends).  The
  *     caller guarantees that the kernel launched immediately before a call on
  *     its stream does not write those index arrays.  Data (q, k, v, caches,
- *     tables, workspace, out) are always read after the wait. */
+ *     tables, workspace, out) are always read after the wait.
+ *   PA_OVERLAP_EARLY_KV  early metadata, and decode attention (plain, fused
+ *     step, fp8) also starts copying K/V cache rows before the wait: every
+ *     row except each request's newest one (position seq_lens[b] - 1), which
+ *     is read after the wait.  The caller guarantees that the kernel launched
+ *     immediately before a decode call writes no cache row of that call's
+ *     layer other than the requests' newest rows (true in a decode step,
+ *     where that kernel is the new token's projection, RoPE or KV store, or
+ *     another layer's attention).  Other calls behave as in early-metadata
+ *     mode. */
 #define PA_OVERLAP_OFF 0
 #define PA_OVERLAP_SAFE 1
 #define PA_OVERLAP_EARLY_METADATA 2
+#define PA_OVERLAP_EARLY_KV 3
 /* PA_ERR_SHAPE for an unknown mode. */
 pa_status pa_set_launch_overlap(int mode);
 int pa_get_launch_overlap(void);
+
+/* ------------------------------------------------------ wait time limit
+ * Every pipeline wait inside the kernels (a warp waiting for copies or
+ * tensor-core work of its own CTA) gives up after a time limit: the CTA then
+ * sets PA_DEVERR_TIMEOUT, lets the copies and MMAs it has issued finish,
+ * frees its tensor memory and exits, so a stuck pipeline ends the call with
+ * an error instead of a hang.  The limit is process-wide, read at each call
+ * (and frozen into a graph at capture); the default is 2 s.  Setting 0 makes
+ * every wait that finds its phase incomplete give up at once: a test hook
+ * that drives the abort path without any fault (the first copies a kernel
+ * waits for are still in flight when it first looks).  Restore the default
+ * (2000000000) afterwards. */
+void pa_set_wait_timeout_ns(uint64_t ns);
+uint64_t pa_get_wait_timeout_ns(void);
 
 /* ----------------------------------------------------------- workspaces
  * A workspace is one caller-allocated device buffer, 256-byte aligned.  Its
@@ -271,6 +295,21 @@ pa_status pa_paged_decode_attn_fp8(const void *q, int batch, int n_q_heads, cons
                                    void *workspace, size_t workspace_bytes, int max_splits, void *out,
                                    cudaStream_t st);
 
+/* pa_paged_prefill_attn_fp8: pa_paged_prefill_attn over an fp8 cache -- the
+ * same arguments, workspace, limits (head_dim 64 or 128, G in {1, 2, 4, 8,
+ * 16}) and error reporting, plus the two scale arrays; k_buf / v_buf are the
+ * uint8 buffers.  Key j of kv head h is e4m3_value(K[layer_id, slot_j, h, :])
+ * * k_scale[layer_id, h], value rows likewise with v_scale.  The e4m3 tiles
+ * are widened to bf16 in shared memory (exact) before the tcgen05 MMAs, so q
+ * stays bf16 and the arithmetic is that of pa_paged_prefill_attn: the K scale
+ * joins the softmax scale and the V scale multiplies each output row. */
+pa_status pa_paged_prefill_attn_fp8(const void *q, int n_tokens, int n_q_heads, const void *k_buf,
+                                    const void *v_buf, pa_kv_shape s, int layer_id, const int32_t *qo_indptr,
+                                    const int32_t *kv_indptr, int n_reqs, const int32_t *req_to_token, int req_rows,
+                                    int max_ctx, const int32_t *req_pool_indices, float scale, const float *k_scale,
+                                    const float *v_scale, void *workspace, size_t workspace_bytes, void *out,
+                                    cudaStream_t st);
+
 /* ------------------------------------------------------ fused decode step
  * One layer's decode step in one launch (commit 398e8a3: the CUDA-graph
  * decode step over packed inputs, rotary embedding on packed 3-D inputs, K/V
@@ -344,7 +383,7 @@ pa_status pa_paged_decode_attn_cascade(const void *q, int batch, int n_q_heads, 
  * q, out: bf16 [n_tokens, n_q_heads, head_dim]; qo_indptr, kv_indptr: int32
  * [n_reqs + 1] (device), qo_indptr[n_reqs] == n_tokens.  QK^T and PV run on
  * tcgen05 tensor cores (bf16 operands, fp32 accumulation in tensor memory, P
- * rounded to bf16).  Supported: head_dim 128; G in {1, 2, 4, 8, 16}.
+ * rounded to bf16).  Supported: head_dim 64 or 128; G in {1, 2, 4, 8, 16}.
  * n_r > L_r or L_r > max_ctx sets PA_DEVERR_LEN and skips that request. */
 pa_status pa_paged_prefill_attn(const void *q, int n_tokens, int n_q_heads, const void *k_buf,
                                 const void *v_buf, pa_kv_shape s, int layer_id,
@@ -373,7 +412,7 @@ pa_status pa_paged_prefill_attn_last(const void *q, int n_tokens, int n_q_heads,
  * qo_indptr; query i of request r attends to tokens 0..i of request r.
  * Gives the same bits as pa_paged_prefill_attn over a cache holding exactly
  * these rows with no prefix.  last_out as in pa_paged_prefill_attn_last, or
- * NULL.  Supported: head_dim 128, G in {1, 2, 4, 8, 16}, n_reqs <= 2048. */
+ * NULL.  Supported: head_dim 64 or 128, G in {1, 2, 4, 8, 16}, n_reqs <= 2048. */
 pa_status pa_dense_prefill_attn(const void *q, int n_tokens, int n_q_heads, const void *k, const void *v,
                                 int n_kv_heads, int head_dim, const int32_t *qo_indptr, int n_reqs, float scale,
                                 void *workspace, size_t workspace_bytes, void *out, void *last_out,

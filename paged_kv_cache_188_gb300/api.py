@@ -26,7 +26,7 @@ PA_OK = 0
 STATUS = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_SHAPE", 3: "PA_ERR_ALIGN", 4: "PA_ERR_UNSUPPORTED",
           5: "PA_ERR_WORKSPACE", 6: "PA_ERR_CUDA", 7: "PA_ERR_DEVICE_INDEX"}
 DEVERR_SLOT, DEVERR_ROW, DEVERR_LEN, DEVERR_POS = 0x1, 0x2, 0x4, 0x8
-OVERLAP_OFF, OVERLAP_SAFE, OVERLAP_EARLY_METADATA = 0, 1, 2
+OVERLAP_OFF, OVERLAP_SAFE, OVERLAP_EARLY_METADATA, OVERLAP_EARLY_KV = 0, 1, 2, 3
 
 
 class PaError(RuntimeError):
@@ -50,7 +50,8 @@ EXPORTS = ["pa_status_string", "pa_decode_workspace_bytes", "pa_prefill_workspac
            "pa_paged_decode_attn", "pa_paged_prefill_attn", "pa_paged_decode_attn_noalloc",
            "pa_set_launch_overlap", "pa_get_launch_overlap", "pa_decode_step",
            "pa_paged_prefill_attn_last", "pa_dense_prefill_attn", "pa_cascade_workspace_bytes",
-           "pa_paged_decode_attn_cascade", "pa_kv_store_fp8", "pa_paged_decode_attn_fp8"]
+           "pa_paged_decode_attn_cascade", "pa_kv_store_fp8", "pa_paged_decode_attn_fp8",
+           "pa_paged_prefill_attn_fp8", "pa_set_wait_timeout_ns", "pa_get_wait_timeout_ns"]
 
 _lib = None
 
@@ -93,11 +94,17 @@ def lib():
     L.pa_kv_store_fp8.argtypes = [P, P, KvShape, i32, P, P, P, i32, P, P, P, P]
     L.pa_paged_decode_attn_fp8.argtypes = [P, i32, i32, P, P, KvShape, i32, P, i32, i32, P, P, f32, P, P, P, sz,
                                            i32, P, P]
+    L.pa_paged_prefill_attn_fp8.argtypes = [P, i32, i32, P, P, KvShape, i32, P, P, i32, P, i32, i32, P, f32, P, P,
+                                            P, sz, P, P]
     L.pa_set_launch_overlap.argtypes = [i32]
     L.pa_get_launch_overlap.argtypes = []
+    L.pa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    L.pa_get_wait_timeout_ns.argtypes = []
     for name in EXPORTS[3:]:
         getattr(L, name).restype = i32
     L.pa_cascade_workspace_bytes.restype = sz
+    L.pa_set_wait_timeout_ns.restype = None
+    L.pa_get_wait_timeout_ns.restype = ctypes.c_uint64
     _lib = L
     return L
 
@@ -155,7 +162,7 @@ def _kv_shape_fp8(k_buf, v_buf, k_scale, v_scale):
 
 
 def pa_set_launch_overlap(mode):
-    """Process-wide launch overlap (OVERLAP_OFF / OVERLAP_SAFE / OVERLAP_EARLY_METADATA)."""
+    """Process-wide launch overlap (OVERLAP_OFF / OVERLAP_SAFE / OVERLAP_EARLY_METADATA / OVERLAP_EARLY_KV)."""
     _ok("pa_set_launch_overlap", lib().pa_set_launch_overlap(int(mode)))
 
 
@@ -333,6 +340,40 @@ def pa_paged_decode_attn_noalloc(q, k_buf, v_buf, layer_id, req_to_token, req_po
         _p(q), B, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(req_to_token), req_to_token.shape[0],
         req_to_token.shape[1], _p(req_pool_indices), _p(seq_lens), float(scale), max_splits, _p(out),
         _p(error_word), _stream(stream)))
+
+
+WAIT_TIMEOUT_DEFAULT_NS = 2_000_000_000
+
+
+def pa_set_wait_timeout_ns(ns):
+    """Time limit of the kernels' bounded pipeline waits; 0 makes every wait
+    give up at once (a test hook for the abort path)."""
+    lib().pa_set_wait_timeout_ns(int(ns))
+
+
+def pa_get_wait_timeout_ns():
+    return int(lib().pa_get_wait_timeout_ns())
+
+
+def pa_paged_prefill_attn_fp8(q, k_buf, v_buf, layer_id, qo_indptr, kv_indptr, req_to_token, req_pool_indices,
+                              scale, k_scale, v_scale, workspace, out, stream=None):
+    """Ragged causal prefill over an e4m3 cache with per-(layer, kv head) scales."""
+    s = _kv_shape_fp8(k_buf, v_buf, k_scale, v_scale)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(qo_indptr, torch.int32, "qo_indptr", 1)
+    _need(kv_indptr, torch.int32, "kv_indptr", 1)
+    _need(req_to_token, torch.int32, "req_to_token", 2)
+    _need(req_pool_indices, torch.int32, "req_pool_indices", 1)
+    _need(workspace, torch.uint8, "workspace")
+    T, Hq, D = q.shape
+    R = qo_indptr.numel() - 1
+    if out.shape != q.shape or D != s.head_dim or kv_indptr.numel() != R + 1 or req_pool_indices.numel() != R:
+        raise ValueError("q/out [T, Hq, D], qo/kv_indptr [R+1], req_pool_indices [R] expected")
+    _ok("pa_paged_prefill_attn_fp8", lib().pa_paged_prefill_attn_fp8(
+        _p(q), T, Hq, _p(k_buf), _p(v_buf), s, layer_id, _p(qo_indptr), _p(kv_indptr), R, _p(req_to_token),
+        req_to_token.shape[0], req_to_token.shape[1], _p(req_pool_indices), float(scale), _p(k_scale), _p(v_scale),
+        _p(workspace), workspace.numel(), _p(out), _stream(stream)))
 
 
 def pa_paged_prefill_attn(q, k_buf, v_buf, layer_id, qo_indptr, kv_indptr, req_to_token, req_pool_indices,

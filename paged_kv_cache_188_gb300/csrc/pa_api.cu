@@ -13,6 +13,12 @@ static volatile int g_overlap = PA_OVERLAP_OFF;
 
 int launch_overlap() { return g_overlap; }
 
+static volatile uint64_t g_wait_ns = 2000000000ull;
+
+uint64_t wait_limit_ns() { return g_wait_ns; }
+
+bool early_metadata() { return g_overlap == PA_OVERLAP_EARLY_METADATA || g_overlap == PA_OVERLAP_EARLY_KV; }
+
 int num_sms()
 {
     static int cached[64] = {0};
@@ -75,15 +81,26 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-bool encode_tmap_bf16(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                      const cuuint32_t *box)
+static bool encode_tmap(CUtensorMap *m, CUtensorMapDataType dtype, CUtensorMapSwizzle swizzle, const void *ptr,
+                        int rank, const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(m, dtype, rank, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_bf16(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                      const cuuint32_t *box)
+{
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, ptr, rank, dims, strides, box);
+}
+
+bool encode_tmap_u8(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                    const cuuint32_t *box)
+{
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE, ptr, rank, dims, strides, box);
 }
 
 DecodeWsLayout decode_ws_layout(size_t workspace_bytes, int n_q_heads, int n_kv_heads, int head_dim,
@@ -159,9 +176,15 @@ extern "C" pa_status pa_get_error(const void *workspace, int32_t *device_error, 
 
 extern "C" pa_status pa_set_launch_overlap(int mode)
 {
-    if (mode != PA_OVERLAP_OFF && mode != PA_OVERLAP_SAFE && mode != PA_OVERLAP_EARLY_METADATA) return PA_ERR_SHAPE;
+    if (mode != PA_OVERLAP_OFF && mode != PA_OVERLAP_SAFE && mode != PA_OVERLAP_EARLY_METADATA &&
+        mode != PA_OVERLAP_EARLY_KV)
+        return PA_ERR_SHAPE;
     pa::g_overlap = mode;
     return PA_OK;
 }
 
 extern "C" int pa_get_launch_overlap(void) { return pa::g_overlap; }
+
+extern "C" void pa_set_wait_timeout_ns(uint64_t ns) { pa::g_wait_ns = ns; }
+
+extern "C" uint64_t pa_get_wait_timeout_ns(void) { return pa::g_wait_ns; }

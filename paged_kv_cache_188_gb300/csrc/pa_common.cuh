@@ -124,6 +124,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two)
     return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
+// Two e4m3 bytes (the low one first) -> bf16x2.  Exact: every e4m3 value is
+// a bf16 number (3 significant bits, exponents -9 .. 8).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+    __half_raw lo, hi;
+    lo.x = h.x;
+    hi.x = h.y;
+    return pack_bf16x2(__half2float(__half(lo)), __half2float(__half(hi)));
+}
+
 // bf16x2 word -> f16x2 word, each value clamped to the f16 range first (f16
 // holds bf16's 8 significant bits; magnitudes below 2^-14 lose low bits).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t w)

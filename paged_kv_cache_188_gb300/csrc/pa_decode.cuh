@@ -113,6 +113,8 @@ struct DecodeArgs {
     int cap_batch, max_splits;
     int layer_row0;      // layer_id * size: tensor-map row of slot 0 of the layer
     int early_meta;      // launched behind another kernel: plan and page table before waiting for it
+    int early_kv;        // ... and copy K/V tiles (not the requests' newest rows) before waiting for it
+    uint64_t wait_ns;    // time limit of the ring waits
     float scale_log2;
     // fused decode step (k_new != null): RoPE on q as it is loaded, and the new
     // token's rotated K and its V written at loc[b] before any tile is read
@@ -321,6 +323,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     // the suffix launch plans from req_start, which the prefix launch writes:
     // it never plans before its wait
     const bool early = a.early_meta && MODE != MODE_SUFFIX;
+    const bool early_kv = early && a.early_kv && (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8);
     constexpr int KSTEPS = D / 16;
     constexpr int DM = D / 16;         // 16-row d tiles of O^T
     constexpr int CPR = D / 8;         // 16-byte chunks per row
@@ -402,6 +405,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     const int64_t slot_stride = (int64_t)Hkv * D;
     const uint32_t ring = smem_u32(smem) + warp * L::kRing;
     bool bad = false;   // a ring wait timed out: skip work, keep the barriers
+    int ring_err = 0;   // error bits found while loading tiles, written at the end (some precede the wait)
 
     // ------------------------------------------- this warp's load cursors
     // a cursor walks (item, tile) pairs in the order the warp computes them:
@@ -444,7 +448,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         const int tok0 = cur.I.t0 + cur.tile * kDecTile;
         int sl = cur.slot;
         const bool in_range = lane < kDecTile && tok0 + lane < cur.I.t1;
-        if (in_range && (sl < 0 || sl >= a.size)) set_error(a.err, PA_DEVERR_SLOT);
+        if (in_range && (sl < 0 || sl >= a.size)) ring_err |= PA_DEVERR_SLOT;
         const bool ok = in_range && sl >= 0 && sl < a.size;
         if (!ok) sl = -1;
         const unsigned vmask = __ballot_sync(0xffffffffu, ok);
@@ -562,6 +566,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             reinterpret_cast<uint4 *>(dst)[c] = x;
         }
     };
+    // early K/V: a warp's first tiles are copied before the wait, stopping at
+    // the first tile that holds a request's newest token (the last tile of
+    // its last split), which the preceding kernel or this CTA may write
+    int pre = 0;
+    if (early_kv) {
+        while (pre < S - 1 && cur.item < total_items && !(cur.I.s == cur.I.sb - 1 && cur.tile == cur.I.ntiles - 1)) {
+            issue();
+            ++pre;
+        }
+    }
     bool more_steps = false;
     if (FUSED) more_steps = collect(0);
     if (early) pdl_wait();
@@ -598,8 +612,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         fence_proxy_async_global();
         __syncthreads();
     }
-#pragma unroll
-    for (int i = 0; i < S - 1; ++i) issue();
+    for (; pre < S - 1; ++pre) issue();
 
     // ------------------------------------------------------ split merge
     // The CTA whose ticket completes (b, h) merges all its splits in split
@@ -733,7 +746,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         if (s_flag) merge_splits(s_pend[0], s_pend[1], s_pend[2]);
     };
 
-    int n_done = 0;   // tiles computed by this warp
+    int n_done = 0;   // tiles computed (or, after a timed-out wait, skipped) by this warp
+    int n_landed = 0; // tiles whose ring wait succeeded: those after it may still be in flight
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
         const DecItem I = dec_item<MODE>(a, s_pref, chunk, item);
         const int hq0 = I.h * G;
@@ -839,7 +853,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         for (int i = warp; i < I.ntiles; i += kDecWarps) {
             if (!bad) issue();
             const int st = n_done % S;
-            if (!bad && !mbar_wait(bars + st * 8, (n_done / S) & 1, s_abort, a.err, PA_DEVERR_TIMEOUT)) bad = true;
+            if (!bad && !mbar_wait(bars + st * 8, (n_done / S) & 1, s_abort, a.err, PA_DEVERR_TIMEOUT, a.wait_ns))
+                bad = true;
+            if (!bad) ++n_landed;
             ++n_done;
             if (bad) continue;
             const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile;
@@ -1115,12 +1131,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     if (bad || *s_abort) {
         // aborted: let this warp's loads already in flight land before the
         // CTA's shared memory goes away (bounded, 10 ms per stage)
-        for (int j = n_done; j < n_issued; ++j) {
-            const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(bars + (j % S) * 8, (j / S) & 1) && global_ns() - t0 < 10000000ull) {
-            }
-        }
+        for (int j = n_landed; j < n_issued; ++j) mbar_drain(bars + (j % S) * 8, (j / S) & 1);
     }
+    if (ring_err) set_error(a.err, ring_err);
 }
 
 template <int D, int S, int NH, int MODE>
@@ -1240,7 +1253,9 @@ static bool fill_decode_args(DecodeArgs &a, const void *q, int batch, int n_q_he
     a.cap_batch = ws.cap_batch;
     a.max_splits = max_splits;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    a.early_meta = launch_overlap() == PA_OVERLAP_EARLY_METADATA;
+    a.early_meta = early_metadata();
+    a.early_kv = launch_overlap() == PA_OVERLAP_EARLY_KV;
+    a.wait_ns = wait_limit_ns();
     return true;
 }
 

@@ -34,6 +34,13 @@ bool ensure_dynamic_smem(const void *kern, size_t bytes);
 // Current launch-overlap mode (PA_OVERLAP_*).
 int launch_overlap();
 
+// Time limit of the kernels' bounded pipeline waits (pa_set_wait_timeout_ns).
+uint64_t wait_limit_ns();
+
+// Index arrays may be read before the wait for the preceding kernel
+// (PA_OVERLAP_EARLY_METADATA, and PA_OVERLAP_EARLY_KV which includes it).
+bool early_metadata();
+
 // Launch `kern` on `st`, as a programmatic dependent of the preceding kernel
 // when launch overlap is on.
 template <typename... KArgs, typename... Args>
@@ -59,6 +66,11 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 // resolved once through the runtime (no libcuda link).  false on failure.
 bool encode_tmap_bf16(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
                       const cuuint32_t *box);
+
+// The same over a byte tensor (e4m3 cache rows) without swizzle: a box lands
+// in shared memory as plain rows.
+bool encode_tmap_u8(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                    const cuuint32_t *box);
 
 // Decode workspace geometry, a pure function of its arguments.
 struct DecodeWsLayout {

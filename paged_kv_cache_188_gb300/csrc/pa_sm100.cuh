@@ -47,24 +47,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase of `bar` with the given parity to complete.  Gives up
-// after `limit_ns` nanoseconds or as soon as *abort is set; on a time-out it
-// raises *abort and ORs `err_bit` into the device error word.  Returns true
-// when the phase completed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *err,
-                                          int err_bit, uint64_t limit_ns = 2000000000ull)
+// Slow path of mbar_wait: spin until the phase completes, *abort is set, or
+// `limit_ns` nanoseconds pass (then raise *abort and OR `err_bit` into the
+// device error word).  limit_ns == 0 gives up at once.  Kept out of line so
+// the fast path (the first probe) carries nothing of it.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *err,
+                                            int err_bit, uint64_t limit_ns)
 {
-    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (limit_ns != 0 && mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (global_ns() - t0 > limit_ns) {
+        if (limit_ns == 0 || global_ns() - t0 > limit_ns) {
             *abort = 1;
             set_error(err, err_bit);
             return false;
         }
     }
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// after `limit_ns` nanoseconds or as soon as *abort is set; on a time-out it
+// raises *abort and ORs `err_bit` into the device error word.  Returns true
+// when the phase completed.  A phase already complete at the first probe is
+// taken without looking at the limit; limit_ns == 0 makes every wait that has
+// to wait give up at once (the host's test setting for the abort path).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *err,
+                                          int err_bit, uint64_t limit_ns = 2000000000ull)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, err, err_bit, limit_ns);
+}
+
+// Wait up to 10 ms for a phase to complete, ignoring any abort: used on the
+// way out of an aborted kernel, for copies or MMAs already issued, which
+// always finish.  Returns true when the phase completed.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > 10000000ull) return false;
+    return true;
 }
 
 // Non-blocking test of a phase: true when the phase with the given parity has completed.
@@ -94,6 +117,11 @@ __device__ __forceinline__ bool mbar_wait_all(const uint32_t (&bar)[N], const ui
 #pragma unroll
     for (int i = 0; i < N; ++i) all &= done[i];
     if (all) return true;
+    if (limit_ns == 0) {
+        *abort = 1;
+        set_error(err, err_bit);
+        return false;
+    }
     const uint64_t t0 = global_ns();
     while (true) {
         all = 1;

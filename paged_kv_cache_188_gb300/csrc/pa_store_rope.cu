@@ -158,7 +158,7 @@ extern "C" pa_status pa_kv_store(void *k_buf, void *v_buf, pa_kv_shape s, int la
                       static_cast<uint4 *>(k_buf) + layer_off, static_cast<uint4 *>(v_buf) + layer_off,
                       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), loc, n_chunks,
                       row_chunks, s.size, error_word,
-                      (int)(launch_overlap() == PA_OVERLAP_EARLY_METADATA)) != cudaSuccess)
+                      (int)early_metadata()) != cudaSuccess)
         return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -185,7 +185,7 @@ extern "C" pa_status pa_kv_store_fp8(void *k_buf, void *v_buf, pa_kv_shape s, in
                       static_cast<uint4 *>(k_buf) + layer_off, static_cast<uint4 *>(v_buf) + layer_off,
                       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), loc, k_scale + scale_off,
                       v_scale + scale_off, n_chunks, row_chunks, s.head_dim / 16, s.size, error_word,
-                      (int)(launch_overlap() == PA_OVERLAP_EARLY_METADATA)) != cudaSuccess)
+                      (int)early_metadata()) != cudaSuccess)
         return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -207,7 +207,7 @@ extern "C" pa_status pa_rope_packed(void *q, int n_q_heads, void *k, int n_kv_he
     if (launch_kernel(rope_kernel, dim3(grid_for(n_chunks, 256)), dim3(256), 0, st, static_cast<uint4 *>(q),
                       static_cast<uint4 *>(k), n_q_heads, n_kv_heads, head_chunks, positions, n_chunks,
                       reinterpret_cast<const float4 *>(cos_tab), reinterpret_cast<const float4 *>(sin_tab), max_pos,
-                      error_word, (int)(launch_overlap() == PA_OVERLAP_EARLY_METADATA)) != cudaSuccess)
+                      error_word, (int)early_metadata()) != cudaSuccess)
         return PA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

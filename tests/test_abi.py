@@ -110,10 +110,10 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 def test_launch_overlap_mode_switch(lib):
     assert api.pa_get_launch_overlap() == api.OVERLAP_OFF
     try:
-        for m in (api.OVERLAP_SAFE, api.OVERLAP_EARLY_METADATA, api.OVERLAP_OFF):
+        for m in (api.OVERLAP_SAFE, api.OVERLAP_EARLY_METADATA, api.OVERLAP_EARLY_KV, api.OVERLAP_OFF):
             api.pa_set_launch_overlap(m)
             assert api.pa_get_launch_overlap() == m
-        assert lib.pa_set_launch_overlap(3) == 2
+        assert lib.pa_set_launch_overlap(4) == 2
         assert lib.pa_set_launch_overlap(-1) == 2
         assert api.pa_get_launch_overlap() == api.OVERLAP_OFF   # a rejected mode changes nothing
     finally:
@@ -148,7 +148,8 @@ def test_prefill_variants_host_validation(lib):
     dense = lambda **kw: lib.pa_dense_prefill_attn(P(FAKE), 10, kw.get("hq", 8), P(FAKE), P(FAKE), kw.get("hkv", 2),
                                                    kw.get("d", 128), P(FAKE), 1, 0.1, P(kw.get("ws", FAKE)), ws_bytes,
                                                    P(FAKE), P(kw.get("last", 0)), None)
-    assert dense(d=64) == 4
+    assert dense(d=96) == 4
+    assert dense(d=32) == 4
     assert dense(hq=6, hkv=4) == 2
     assert dense(ws=0) == 1
     assert dense(last=FAKE + 8) == 3
@@ -237,3 +238,32 @@ def test_noalloc_validation_runs_before_any_cuda_call(lib):
     assert call(batch=4000, hq=32, s=_shape(hkv=8, d=128), splits=64) == 5   # beyond the 16 MiB array
     assert call(err=FAKE + 2) == 3
     assert call(batch=0, q=0, out=0) == 0
+
+
+def test_wait_timeout_hook_round_trip(lib):
+    assert api.pa_get_wait_timeout_ns() == api.WAIT_TIMEOUT_DEFAULT_NS
+    try:
+        api.pa_set_wait_timeout_ns(0)
+        assert api.pa_get_wait_timeout_ns() == 0
+        api.pa_set_wait_timeout_ns(12345)
+        assert api.pa_get_wait_timeout_ns() == 12345
+    finally:
+        api.pa_set_wait_timeout_ns(api.WAIT_TIMEOUT_DEFAULT_NS)
+    assert api.pa_get_wait_timeout_ns() == api.WAIT_TIMEOUT_DEFAULT_NS
+
+
+def test_prefill_fp8_host_validation(lib):
+    P = ctypes.c_void_p
+    ws_bytes = api.pa_prefill_workspace_bytes()
+
+    def call(d=128, hq=8, ks=FAKE, vs=FAKE, n=10, ws=FAKE):
+        return lib.pa_paged_prefill_attn_fp8(P(FAKE), n, hq, P(FAKE), P(FAKE), api.KvShape(1, 64, 2, d), 0, P(FAKE),
+                                             P(FAKE), 1, P(FAKE), 1, 16, P(FAKE), 0.1, P(ks) if ks else None,
+                                             P(vs) if vs else None, P(ws), ws_bytes, P(FAKE), None)
+    assert call(d=96) == 4
+    assert call(hq=7) == 2
+    assert call(hq=6) == 4                        # G = 3
+    assert call(ks=0) == 1
+    assert call(vs=FAKE + 2) == 3
+    assert call(ws=FAKE + 16) == 3
+    assert call(n=0, ks=0, vs=0) == 0

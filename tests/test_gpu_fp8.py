@@ -182,3 +182,68 @@ def test_config2_full_size_fp8(seq_len):
     ref = oracle.decode_fp8(bits(st.q), kh, vh, 0, r2t, np.zeros(1, np.int32), np.array([seq_len], np.int32),
                             st.scale, l_ks, l_vs)
     assert_attention_close(npy(out.float()), ref, f"fp8 config 2 seq {seq_len}")
+
+
+# ------------------------------------------------------------ fp8 prefill
+
+def _prefill_fp8_case(new, pre, Hq, Hkv, D, page, seed, size=8192):
+    """A packed prefill batch over an e4m3 cache: the generator's bf16 cache
+    quantised whole by the library's store (and by the oracle on the host),
+    then the new tokens' K/V stored quantised at their slots on both sides."""
+    pb = W.make_prefill_batch(new_lens=new, prefix_lens=pre, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D,
+                              size=size, page_size=page, seed=seed, req_rows=len(new) + 3, device="cuda")
+    ks, vs = _scales(1, Hkv, seed)
+    k8, v8, ksd, vsd, kh, vh = _quantise_cache(pb.kv, ks, vs)
+    api.pa_kv_store_fp8(k8, v8, pb.layer, pb.k_new, pb.v_new, pb.loc, ksd, vsd)
+    kh, vh = oracle.kv_store_fp8(kh, vh, pb.layer, bits(pb.k_new), bits(pb.v_new), npy(pb.loc), npy(ks), npy(vs))
+    return pb, k8, v8, ksd, vsd, kh, vh, ks, vs
+
+
+def _prefill_fp8(pb, k8, v8, ksd, vsd, ws=None):
+    ws = api.alloc_workspace(api.pa_prefill_workspace_bytes()) if ws is None else ws
+    out = torch.full_like(pb.q, float("nan"))
+    api.pa_paged_prefill_attn_fp8(pb.q, k8, v8, pb.layer, pb.qo_indptr, pb.kv_indptr, pb.kv.req_to_token,
+                                  pb.kv.req_pool_indices, pb.scale, ksd, vsd, ws, out)
+    torch.cuda.synchronize()
+    assert api.pa_get_error(ws) == 0
+    return out, ws
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("D,page", [(128, 16), (64, 1)])
+def test_prefill_fp8_ragged(G, D, page):
+    """Ragged prompts with and without cached prefixes, lengths around the
+    128-row q and kv tile edges, G = 1 .. 16, head_dim 64 and 128, page
+    sizes 16 (box gathers) and 1 (row gathers)."""
+    new, pre = [1, 31, 130, 7, 300, 128], [0, 5, 300, 17, 1000, 129]
+    pb, k8, v8, ksd, vsd, kh, vh, ks, vs = _prefill_fp8_case(new, pre, 2 * G, 2, D, page, seed=G * 13 + D + page)
+    out, _ = _prefill_fp8(pb, k8, v8, ksd, vsd)
+    ref = oracle.prefill_fp8(bits(pb.q), kh, vh, pb.layer, npy(pb.qo_indptr), npy(pb.kv_indptr),
+                             npy(pb.kv.req_to_token), npy(pb.kv.req_pool_indices), pb.scale, npy(ks), npy(vs))
+    assert_attention_close(npy(out.float()), ref, f"fp8 prefill G={G} D={D} page={page}")
+
+
+def test_prefill_fp8_config4_shape_sampled_and_deterministic():
+    """Config 4's prompt lengths, heads and cache over an e4m3 copy: every
+    head of the first, last and 4 random rows of each request against the
+    oracle, and two calls bit-identical."""
+    pb = W.config4(device="cuda")
+    ks, vs = _scales(1, 8, 4)
+    k8, v8, ksd, vsd, kh, vh = _quantise_cache(pb.kv, ks, vs)
+    api.pa_kv_store_fp8(k8, v8, pb.layer, pb.k_new, pb.v_new, pb.loc, ksd, vsd)
+    kh, vh = oracle.kv_store_fp8(kh, vh, pb.layer, bits(pb.k_new), bits(pb.v_new), npy(pb.loc), npy(ks), npy(vs))
+    out1, ws = _prefill_fp8(pb, k8, v8, ksd, vsd)
+    out2, _ = _prefill_fp8(pb, k8, v8, ksd, vsd, ws=ws)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    qo = npy(pb.qo_indptr)
+    rng = np.random.default_rng(44)
+    rows = []
+    for r in range(len(pb.new_lens)):
+        rows += [qo[r], qo[r + 1] - 1] + rng.integers(qo[r], qo[r + 1], 4).tolist()
+    rows = sorted(set(int(x) for x in rows))
+    Hq = pb.q.shape[1]
+    st = np.repeat(np.array(rows, np.int32), Hq)
+    sh = np.tile(np.arange(Hq, dtype=np.int32), len(rows))
+    ref = oracle.prefill_fp8(bits(pb.q), kh, vh, pb.layer, qo, npy(pb.kv_indptr), npy(pb.kv.req_to_token),
+                             npy(pb.kv.req_pool_indices), pb.scale, npy(ks), npy(vs), sel=(st, sh))
+    assert_attention_close(npy(out1.float())[st, sh], ref, "fp8 prefill, config 4 sampled")

@@ -2,8 +2,10 @@
 never what they compute: chains in which each call reads what the previous
 call wrote -- RoPE -> KV store -> decode, RoPE -> KV store -> prefill, and
 back-to-back decodes sharing one workspace -- give bit-identical results with
-overlap off, safe, and early-metadata, eagerly and under repeated graph
-replay."""
+overlap off, safe, early-metadata and early-KV, eagerly and under repeated graph
+replay.  Early-KV mode copies cache rows other than each request's newest
+one before the wait, which these chains allow (the store writes only the
+newest rows)."""
 import pytest
 import torch
 
@@ -11,7 +13,7 @@ from paged_kv_cache_188_gb300 import api
 from paged_kv_cache_188_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
-MODES = [api.OVERLAP_OFF, api.OVERLAP_SAFE, api.OVERLAP_EARLY_METADATA]
+MODES = [api.OVERLAP_OFF, api.OVERLAP_SAFE, api.OVERLAP_EARLY_METADATA, api.OVERLAP_EARLY_KV]
 
 
 @pytest.fixture(autouse=True)

@@ -55,6 +55,35 @@ def test_ragged_small(G, page):
     assert api.pa_get_error(ws) == 0
 
 
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("page", [16, 1])
+def test_ragged_small_head_dim_64(G, page):
+    new = [1, 31, 32, 33, 130, 7, 300]
+    pre = [0, 5, 128, 0, 300, 17, 1000]
+    pb = W.make_prefill_batch(new_lens=new, prefix_lens=pre, n_q_heads=2 * G, n_kv_heads=2, head_dim=64,
+                              size=4096, page_size=page, seed=G * 10 + page + 64, req_rows=9, device="cuda")
+    kb, vb = _store(pb)
+    out, ws = _run(pb)
+    assert_attention_close(npy(out.float()), _ref(pb, kb, vb), f"prefill D=64 G={G} page={page}")
+    assert api.pa_get_error(ws) == 0
+
+
+@pytest.mark.parametrize("G", [1, 4, 16])
+def test_dense_prefill_head_dim_64(G):
+    new = [1, 17, 300, 128, 700]
+    pb = W.make_prefill_batch(new_lens=new, prefix_lens=[0] * len(new), n_q_heads=2 * G, n_kv_heads=2,
+                              head_dim=64, size=4096, page_size=16, seed=70 + G, device="cuda")
+    kb, vb = _store(pb)
+    ref, _ = _run(pb)
+    ws = api.alloc_workspace(api.pa_prefill_workspace_bytes())
+    out = torch.full_like(pb.q, float("nan"))
+    api.pa_dense_prefill_attn(pb.q, pb.k_new, pb.v_new, pb.qo_indptr, pb.scale, ws, out)
+    torch.cuda.synchronize()
+    assert api.pa_get_error(ws) == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert_attention_close(npy(out.float()), _ref(pb, kb, vb), f"dense prefill D=64 G={G}")
+
+
 def test_mixed_pages_and_long_prefix():
     # page size 4: 16-position groups are never one contiguous page -> per-row boxes
     new, pre = [200, 64, 1000], [1024, 0, 40]
