@@ -51,7 +51,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 // `limit_ns` nanoseconds pass (then raise *abort and OR `err_bit` into the
 // device error word).  limit_ns == 0 gives up at once.  Kept out of line so
 // the fast path (the first probe) carries nothing of it.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *err,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort, int32_t *err,
                                             int err_bit, uint64_t limit_ns)
 {
     const uint64_t t0 = global_ns();
