@@ -435,6 +435,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     cur.I.row = -1;
     cur.I.t0 = cur.I.t1 = cur.I.h = 0;
     if (cur.item < total_items) cur.I = dec_item<MODE>(a, s_pref, chunk, cur.item);
+    // the CTA's first item, kept for the item loop: in early-metadata mode it
+    // is derived before the wait, so the loop's first iteration re-reads nothing
+    const DecItem first_I = cur.I;
     settle(cur);
     Cursor nxt = cur;
     nxt.tile += kDecWarps;
@@ -748,9 +751,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
 
     int n_done = 0;   // tiles computed (or, after a timed-out wait, skipped) by this warp
     int n_landed = 0; // tiles whose ring wait succeeded: those after it may still be in flight
+    bool ticket_pending = false;   // CTA-uniform: the previous item took a merge ticket
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const DecItem I = dec_item<MODE>(a, s_pref, chunk, item);
+        const DecItem I = item == (int)blockIdx.x ? first_I : dec_item<MODE>(a, s_pref, chunk, item);
         const int hq0 = I.h * G;
+        if (a.wait_ns == 0 && !bad) {
+            // a wait limit of 0: give up at the first item, as a timed-out ring wait would
+            *s_abort = 1;
+            set_error(a.err, PA_DEVERR_TIMEOUT);
+            bad = true;
+        }
         // Q^T as the MMA's B operand: n = head (8 per n-tile), k = d
         uint32_t qb[KSTEPS][NH][2];
         {
@@ -1033,7 +1043,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         // scratch free (the previous item is done with it); all warps stop
         // together if any ring wait timed out
         if (__syncthreads_or(bad)) break;
-        resolve_ticket();   // the previous item's split merge, if this CTA completed it
+        if (ticket_pending) resolve_ticket();   // the previous item's split merge, if this CTA completed it
+        ticket_pending = false;
         if (g == 0) {
 #pragma unroll
             for (int nt = 0; nt < NH; ++nt)
@@ -1046,15 +1057,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                     }
                 }
         }
-        // O states go through the scratch in two rounds (warps 0-3, then 4-7);
-        // every element still sums warps 0..7 in order with the same weights
+        // O states go through the scratch in one round when all eight warps'
+        // G rows fit (G <= 4 NH), else in two (warps 0-3, then 4-7); either
+        // way every element sums warps 0..7 in order with the same weights
         constexpr int EPT = (8 * NH * D + kDecThreads - 1) / kDecThreads;
+        const bool one_round = G <= 4 * NH;
+        const int wpr = one_round ? kDecWarps : kDecWarps / 2;   // warps per round
         float acc[EPT], lsum[EPT], Mx[EPT];
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
+            if (rr == 1 && one_round) break;
             if (rr == 1) __syncthreads();   // round 0 readers are done with the scratch
-            if ((warp >> 2) == rr) {
-                const int wl = warp & 3;
+            if (one_round || (warp >> 2) == rr) {
+                const int wl = one_round ? warp : warp & 3;
 #pragma unroll
                 for (int dm = 0; dm < DM; ++dm)
 #pragma unroll
@@ -1082,7 +1097,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 }
                 const float Mr = Mx[k] == -INFINITY ? 0.f : Mx[k];
 #pragma unroll
-                for (int w = 0; w < kDecWarps / 2; ++w) {
+                for (int w = 0; w < kDecWarps; ++w) {
+                    if (w >= wpr) break;
                     const int wg = rr * (kDecWarps / 2) + w;
                     const float wt = ex2(s_m[wg][gg] - Mr);
                     lsum[k] += wt * s_l[wg][gg];
@@ -1119,6 +1135,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             // the next item end (or at exit), so the round trip overlaps the
             // next item's tiles
             __syncthreads();
+            ticket_pending = true;
             if (tid == 0) {
                 pend_prev = atom_add_acq_rel_gpu(a.counters + I.b * Hkv + I.h, 1);
                 s_pend[0] = I.b;
@@ -1127,7 +1144,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             }
         }
     }
-    if (!bad && !*s_abort) resolve_ticket();
+    if (!bad && !*s_abort && ticket_pending) resolve_ticket();
     if (bad || *s_abort) {
         // aborted: let this warp's loads already in flight land before the
         // CTA's shared memory goes away (bounded, 10 ms per stage)
