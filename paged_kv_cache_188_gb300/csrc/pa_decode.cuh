@@ -173,7 +173,11 @@ __device__ __forceinline__ void split_of(int n, const DecPlan &pl, int max_split
         s = (n + pl.chunk - 1) / pl.chunk;
     }
     if (s > max_splits) s = max_splits;
-    len = ((n + s - 1) / s + 15) & ~15;
+    // whole rounds of 16-token tiles for the 8 warps: every warp of the item
+    // gets the same number of tiles (8K at 19 splits gave 27 tiles per item,
+    // four warps of four and four of three)
+    constexpr int kRound = kDecWarps * kDecTile;
+    len = ((n + s - 1) / s + kRound - 1) / kRound * kRound;
     sb = (n + len - 1) / len;
 }
 
