@@ -117,10 +117,9 @@ int pa_get_launch_overlap(void);
  * frees its tensor memory and exits, so a stuck pipeline ends the call with
  * an error instead of a hang.  The limit is process-wide, read at each call
  * (and frozen into a graph at capture); the default is 2 s.  Setting 0 makes
- * every wait that finds its phase incomplete give up at once: a test hook
- * that drives the abort path without any fault (the first copies a kernel
- * waits for are still in flight when it first looks).  Restore the default
- * (2000000000) afterwards. */
+ * each decode or prefill CTA give up at its first work item, exactly as if a
+ * wait had timed out there: a test hook that drives the abort path without
+ * any fault.  Restore the default (2000000000) afterwards. */
 void pa_set_wait_timeout_ns(uint64_t ns);
 uint64_t pa_get_wait_timeout_ns(void);
 

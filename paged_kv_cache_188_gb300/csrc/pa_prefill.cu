@@ -610,6 +610,14 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(ITEM_EMPTY + n % kRing));
             if (I.end) break;
+            if (p.wait_ns == 0) {
+                // a wait limit of 0: give up at the first item, as a timed-out
+                // wait would; the other roles then find their next phase
+                // incomplete and see the abort flag
+                *s_abort = 1;
+                set_error(err, PA_DEVERR_TIMEOUT);
+                break;
+            }
             const int nq = X ? I.nqb : I.nqa;
             if (nq <= 0) continue;                // no tile B in this pair
             const int q0 = I.q0 + X * p.TQ;
