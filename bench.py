@@ -71,7 +71,8 @@ def parse():
     p.add_argument("--only-main", action="store_true", help="skip the secondary workloads")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--no-fp8", action="store_true", help="skip the sweep over an e4m3 copy of the cache")
-    p.add_argument("--profile", choices=["decode", "prefill", "prefill_fp8", "rope", "store"], default=None,
+    p.add_argument("--profile", choices=["decode", "decode_shared_prefix", "prefill", "prefill_fp8", "rope", "store"],
+                   default=None,
                    help="run a small fixed case of one kernel (for ncu captures) and exit")
     return p.parse_args()
 
@@ -763,6 +764,23 @@ def run_profile_case(args):
         torch.cuda.synchronize()
         print(json.dumps({"profile": "decode", "launches": 5, "algorithmic_bytes_per_launch":
                           4 * decode_bytes(32768), "device_error_word": api.pa_get_error(ws)}))
+    elif args.profile == "decode_shared_prefix":
+        # B=32 requests in 4 groups of 8 sharing 1024-token prefixes, one layer
+        # (1 GiB of K/V): plain decode, which reads each shared page once per member
+        st = W.config3(device=dev)
+        api.pa_kv_store(st.kv.k_buf, st.kv.v_buf, 0, st.k_new, st.v_new, st.loc)
+        B = st.q.shape[0]
+        ws = api.alloc_workspace(api.pa_decode_workspace_bytes(B, HQ, HKV, D, MAX_SPLITS), dev)
+        out = torch.empty_like(st.q)
+        for _ in range(3):
+            api.pa_paged_decode_attn(st.q, st.kv.k_buf, st.kv.v_buf, 0, st.kv.req_to_token, st.kv.req_pool_indices,
+                                     st.kv.seq_lens, st.scale, ws, MAX_SPLITS, out, stream=s)
+        torch.cuda.synchronize()
+        lens = st.kv.seq_lens.cpu().tolist()
+        unique = (st.kv.used_slots.numel() + B) * HKV * D * 4
+        print(json.dumps({"profile": "decode_shared_prefix", "launches": 3,
+                          "logical_kv_bytes": sum(lens) * HKV * D * 4, "unique_kv_bytes": unique,
+                          "device_error_word": api.pa_get_error(ws)}))
     elif args.profile == "prefill":
         pb = W.config4(device=dev)
         ws = api.alloc_workspace(api.pa_prefill_workspace_bytes(), dev)

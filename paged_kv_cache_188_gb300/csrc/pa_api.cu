@@ -98,9 +98,11 @@ bool encode_tmap_bf16(CUtensorMap *m, const void *ptr, int rank, const cuuint64_
 }
 
 bool encode_tmap_u8(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                    const cuuint32_t *box)
+                    const cuuint32_t *box, bool swizzle128)
 {
-    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE, ptr, rank, dims, strides, box);
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                       swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, ptr, rank, dims, strides,
+                       box);
 }
 
 DecodeWsLayout decode_ws_layout(size_t workspace_bytes, int n_q_heads, int n_kv_heads, int head_dim,

@@ -460,24 +460,35 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         if (!ok) sl = -1;
         const unsigned vmask = __ballot_sync(0xffffffffu, ok);
         if constexpr (F8) {
-            // D-byte rows, D/16 lanes per row; masked rows zero-filled, not read
+            // 16 tokens on one page: a TMA box of 16 D-byte rows per K / V
+            // tile; otherwise D-byte rows by cp.async, D/16 lanes per row,
+            // masked rows zero-filled, not read
             constexpr int CPR8 = D / 16, TPI8 = 32 / CPR8;
+            const int s0 = __shfl_sync(0xffffffffu, sl, 0);
+            const bool page = (__ballot_sync(0xffffffffu, ok && sl == s0 + lane) & 0xFFFFu) == 0xFFFFu;
             if (lane == 0) {
                 s_vmask[warp * S + st] = vmask;
-                mbar_arrive_expect_tx(fb, 0u);
+                mbar_arrive_expect_tx(fb, page ? 2u * L::kTile : 0u);
             }
             __syncwarp();
-            const uint8_t *kh = a.k8_layer + (int64_t)cur.I.h * D;
-            const uint8_t *vh = a.v8_layer + (int64_t)cur.I.h * D;
+            if (page) {
+                if (lane == 0) {
+                    tma_load_2d(kb, &a.tm_k, cur.I.h * D, a.layer_row0 + s0, fb);
+                    tma_load_2d(vb, &a.tm_v, cur.I.h * D, a.layer_row0 + s0, fb);
+                }
+            } else {
+                const uint8_t *kh = a.k8_layer + (int64_t)cur.I.h * D;
+                const uint8_t *vh = a.v8_layer + (int64_t)cur.I.h * D;
 #pragma unroll
-            for (int j = 0; j < kDecTile / TPI8; ++j) {
-                const int r = j * TPI8 + lane / CPR8;
-                const int ch = lane % CPR8;
-                const int rs = __shfl_sync(0xffffffffu, sl, r);
-                const int64_t off = rs >= 0 ? (int64_t)rs * slot_stride + ch * 16 : 0;
-                const int nb = rs >= 0 ? 16 : 0;
-                cp_async_16(kb + L::off8(r, ch), kh + off, nb);
-                cp_async_16(vb + L::off8(r, ch), vh + off, nb);
+                for (int j = 0; j < kDecTile / TPI8; ++j) {
+                    const int r = j * TPI8 + lane / CPR8;
+                    const int ch = lane % CPR8;
+                    const int rs = __shfl_sync(0xffffffffu, sl, r);
+                    const int64_t off = rs >= 0 ? (int64_t)rs * slot_stride + ch * 16 : 0;
+                    const int nb = rs >= 0 ? 16 : 0;
+                    cp_async_16(kb + L::off8(r, ch), kh + off, nb);
+                    cp_async_16(vb + L::off8(r, ch), vh + off, nb);
+                }
             }
         } else {
             // 16 tokens on 16 consecutive slots (one page): four TMA boxes

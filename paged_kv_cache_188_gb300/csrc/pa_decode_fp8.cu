@@ -27,6 +27,17 @@ extern "C" pa_status pa_paged_decode_attn_fp8(const void *q, int batch, int n_q_
                           req_pool_indices, seq_lens, scale, max_splits, out, reinterpret_cast<int32_t *>(w), ws, w,
                           /*bf16_cache=*/false))
         return PA_ERR_CUDA;
+    {
+        // page tiles (16 consecutive slots) move as one TMA box of 16 rows per
+        // K / V tile: D = 128 rows land 128-byte swizzled, as the ring expects;
+        // D = 64 rows land plain
+        const cuuint64_t dims[2] = {(cuuint64_t)s.n_kv_heads * s.head_dim, (cuuint64_t)s.n_layers * s.size};
+        const cuuint64_t strides[1] = {(cuuint64_t)s.n_kv_heads * s.head_dim};
+        const cuuint32_t box[2] = {(cuuint32_t)s.head_dim, kDecTile};
+        if (!encode_tmap_u8(&a.tm_k, k_buf, 2, dims, strides, box, s.head_dim == 128) ||
+            !encode_tmap_u8(&a.tm_v, v_buf, 2, dims, strides, box, s.head_dim == 128))
+            return PA_ERR_CUDA;
+    }
     const int64_t layer_bytes = (int64_t)layer_id * s.size * s.n_kv_heads * s.head_dim;   // one byte per element
     a.k8_layer = static_cast<const uint8_t *>(k_buf) + layer_bytes;
     a.v8_layer = static_cast<const uint8_t *>(v_buf) + layer_bytes;

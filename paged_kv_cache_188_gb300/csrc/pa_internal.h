@@ -67,10 +67,11 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 bool encode_tmap_bf16(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
                       const cuuint32_t *box);
 
-// The same over a byte tensor (e4m3 cache rows) without swizzle: a box lands
-// in shared memory as plain rows.
+// The same over a byte tensor (e4m3 cache rows): without swizzle a box lands
+// in shared memory as plain rows; with swizzle128 (128-byte inner box) it
+// lands in the 128-byte XOR-swizzled layout.
 bool encode_tmap_u8(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                    const cuuint32_t *box);
+                    const cuuint32_t *box, bool swizzle128 = false);
 
 // Decode workspace geometry, a pure function of its arguments.
 struct DecodeWsLayout {
