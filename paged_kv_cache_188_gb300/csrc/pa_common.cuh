@@ -31,6 +31,8 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, int s
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+// Wait until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
 {
@@ -173,6 +175,28 @@ __device__ __forceinline__ uint32_t rope_pair_bf16(uint32_t w, float c, float s)
     const float y0 = fmaf(x0, c, -p0) - e0;
     const float y1 = fmaf(x0, s, p1) + e1;
     return pack_bf16x2(y0, y1);
+}
+
+// Packed pairs of fp32 values (low, high) for the sm_100-family two-float
+// arithmetic; each lane of fma_f32x2 / add_f32x2 is one IEEE round-to-nearest
+// operation, the same value as the scalar fmaf / add.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi)
+{
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
+__device__ __forceinline__ float f32x2_lo(uint64_t x) { return __uint_as_float((uint32_t)x); }
+__device__ __forceinline__ float f32x2_hi(uint64_t x) { return __uint_as_float((uint32_t)(x >> 32)); }
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
 __device__ __forceinline__ float fast_exp2(float x)

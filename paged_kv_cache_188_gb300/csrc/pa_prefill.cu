@@ -116,6 +116,9 @@ struct PrefillParams {
     float scale_log2;
     const float *k_scale;      // fp8 mode: the layer's per-kv-head K / V scales [Hkv]
     const float *v_scale;
+    const __nv_bfloat16 *k_rows;   // bf16 K / V rows (row r at r * row_elems): the cp.async gather
+    const __nv_bfloat16 *v_rows;
+    int row_elems;
     uint64_t wait_ns;          // time limit of the pipeline waits
 };
 
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
     };
     volatile int *s_abort = reinterpret_cast<volatile int *>(sb + PL::kOffMisc);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(sb + PL::kOffMisc + 4);
-    int *s_wsum = reinterpret_cast<int *>(sb + PL::kOffMisc + 8);    // one int per warp
+    int *s_wsum = reinterpret_cast<int *>(sb + PL::kOffMisc + 8);    // one int per warp (at most 12)
     PfItem *s_ring = reinterpret_cast<PfItem *>(sb + PL::kOffRing);
     int *s_pref = reinterpret_cast<int *>(sb + PL::kOffPref);
     auto bar = [&](int i) -> uint32_t { return base + PL::kOffBar + i * 8; };
@@ -400,35 +403,68 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
                             for (int hh = 0; hh < QH; ++hh)
                                 tma_load_2d(dst + hh * kHalf + gi * 16 * 128, m16, col0 + 64 * hh, row, b);
                         }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int rr = 16 * gi + 4 * sub + e;
-                            const int row = okp[e] ? row0 + slot[e] : p.total_rows;
-#pragma unroll
-                            for (int hh = 0; hh < QH; ++hh)
-                                tma_load_2d(dst + hh * kHalf + rr * 128, m1, col0 + 64 * hh, row, b);
-                        }
-                    }
+                    }   // other groups: gathered by cp.async before the barrier arrival
                 };
                 // bf16: the tile lands in its stage; fp8: its e4m3 bytes land
                 // for the widening warp
                 const int kb = F8 ? K_RAW : K_FULL, vb = F8 ? V_RAW : V_FULL;
                 constexpr uint32_t kTileBytes = F8 ? (uint32_t)(kPfKeys * D) : (uint32_t)(QH * kHalf);   // bytes landing
+                // bf16 groups not on one page (page sizes below 16, ragged
+                // ends) are gathered by cp.async, K and V together: the
+                // group's 4 lanes copy 64 contiguous bytes of a row per
+                // instruction into the swizzled tile, the producer waits for
+                // its own copies and fences them for the tensor core's async
+                // proxy before arming the barriers.  Tiles whose groups all
+                // move as TMA boxes (page 16) skip this entirely.
+                const bool gathered = !F8 && !(g_contig || g_empty);
+                const bool any_gathered = __any_sync(0xffffffffu, gathered);
+                uint32_t tile_bytes = kTileBytes;
+                if (any_gathered)
+                    tile_bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, sub == 0 && (g_contig || g_empty))) * 16u *
+                                 (uint32_t)(QH * 128);
+                auto gather = [&](const __nv_bfloat16 *rows, uint32_t dst) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int src_lane = (lane & ~3) + (i >> 2);
+                        const int sl = __shfl_sync(0xffffffffu, slot[i & 3], src_lane);
+                        const bool ok_row = __shfl_sync(0xffffffffu, okp[i & 3], src_lane);
+                        if (!gathered) continue;
+                        const int rr = 16 * gi + i;
+                        const __nv_bfloat16 *src = rows + (int64_t)(row0 + (ok_row ? sl : 0)) * p.row_elems + col0;
+#pragma unroll
+                        for (int q4 = 0; q4 < 2 * QH; ++q4) {
+                            const int ch = q4 * 4 + sub;            // 16-byte chunk of the row (8 per 64 columns)
+                            const int hh = ch >> 3, c = ch & 7;
+                            cp_async_16(dst + hh * kHalf + rr * 128 + ((c ^ (rr & 7)) << 4), src + ch * 8,
+                                        ok_row ? 16 : 0);
+                        }
+                    }
+                };
                 if (kt >= 2 && !wait1(K_EMPTY + st, ph_prev)) {
                     ok = false;
                     break;
                 }
+                if (any_gathered) {
+                    if (kt >= 2 && !wait1(V_EMPTY + st, ph_prev)) {
+                        ok = false;
+                        break;
+                    }
+                    gather(p.k_rows, sK + st * QH * kHalf);
+                    gather(p.v_rows, sV + st * QH * kHalf);
+                    cp_async_wait_all();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
                 ++nk;
-                if (lane == 0) mbar_arrive_expect_tx(bar(kb + st), kTileBytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar(kb + st), tile_bytes);
                 __syncwarp();
                 issue(&p.tm_k16, &p.tm_k1, F8 ? raw_tile(false, st) : sK + st * QH * kHalf, bar(kb + st));
-                if (kt >= 2 && !wait1(V_EMPTY + st, ph_prev)) {
+                if (!any_gathered && kt >= 2 && !wait1(V_EMPTY + st, ph_prev)) {
                     ok = false;
                     break;
                 }
                 ++nv;
-                if (lane == 0) mbar_arrive_expect_tx(bar(vb + st), kTileBytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar(vb + st), tile_bytes);
                 __syncwarp();
                 issue(&p.tm_v16, &p.tm_v1, F8 ? raw_tile(true, st) : sV + st * QH * kHalf, bar(vb + st));
             }
@@ -665,21 +701,26 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
                 const float mb = m_new == -INFINITY ? 0.f : m_new * sl2;
                 // P = exp2(s*scale - m) (masked entries are -inf -> 0), written
                 // back as bf16 pairs over the first 64 columns of S_X
-                float sum0 = 0.f, sum1 = 0.f;
+                // column pairs in packed two-float FMAs and adds (each lane an
+                // IEEE round-to-nearest op: the same values as scalar code)
+                const uint64_t sl2x2 = f32x2_pack(sl2, sl2), nmb2 = f32x2_pack(-mb, -mb);
+                uint64_t sum2 = f32x2_pack(0.f, 0.f);   // even and odd columns' sums
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) {
-                        const float v0 = ex2f(fmaf(__uint_as_float(r[hh * 64 + c]), sl2, -mb));
-                        const float v1 = ex2f(fmaf(__uint_as_float(r[hh * 64 + c + 1]), sl2, -mb));
-                        sum0 += v0;
-                        sum1 += v1;
+                        const uint64_t x = fma_f32x2(f32x2_pack(__uint_as_float(r[hh * 64 + c]),
+                                                                __uint_as_float(r[hh * 64 + c + 1])),
+                                                     sl2x2, nmb2);
+                        const float v0 = ex2f(f32x2_lo(x)), v1 = ex2f(f32x2_hi(x));
+                        const uint64_t v2 = f32x2_pack(v0, v1);
+                        sum2 = add_f32x2(sum2, v2);
                         pk[c / 2] = pack_bf16x2(v0, v1);
                     }
                     tmem_st32(s_addr + hh * 32, pk);
                 }
-                l_run = l_run * alpha + (sum0 + sum1);
+                l_run = l_run * alpha + (f32x2_lo(sum2) + f32x2_hi(sum2));
                 // O_X is stable here: S_X(t) completing implies PV_X(t-1) completed
                 if (t > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -851,6 +892,9 @@ static pa_status prefill_call(const void *q, int n_tokens, int n_q_heads, const 
     prm.early_meta = early_metadata();
     prm.k_scale = k_scale;
     prm.v_scale = v_scale;
+    prm.k_rows = static_cast<const __nv_bfloat16 *>(k_rows);
+    prm.v_rows = static_cast<const __nv_bfloat16 *>(v_rows);
+    prm.row_elems = n_kv_heads * D;
     prm.wait_ns = wait_limit_ns();
 
     if (f8) return D == 64 ? launch_prefill<64, false, false, true>(prm, st) : launch_prefill<128, false, false, true>(prm, st);
