@@ -96,7 +96,7 @@ const char *pa_status_string(pa_status s);
  *   PA_OVERLAP_EARLY_KV  early metadata, and decode attention (plain, fused
  *     step, fp8) also starts copying K/V cache rows before the wait: every
  *     row except each request's newest one (position seq_lens[b] - 1), which
- *     is read after the wait.  The caller guarantees that the kernel launched
+ *     is read after the wait (the fused step takes it from k_new / v_new).  The caller guarantees that the kernel launched
  *     immediately before a decode call writes no cache row of that call's
  *     layer other than the requests' newest rows (true in a decode step,
  *     where that kernel is the new token's projection, RoPE or KV store, or
@@ -324,9 +324,11 @@ pa_status pa_paged_prefill_attn_fp8(const void *q, int n_tokens, int n_q_heads, 
  *   sin_tab: fp32 [max_pos, head_dim / 2].
  *   loc: int32 [batch], the new token's slot.  It must be the request's last
  *   position, loc[b] == req_to_token[req_pool_indices[b], seq_lens[b] - 1]:
- *   the row is written by the one CTA that reads it, just before it reads it.
- *   A mismatch sets PA_DEVERR_SLOT (the row is still written at loc[b]).
- *   k_buf, v_buf: written at [layer_id, loc[b]], then read for attention.
+ *   attention takes that row from k_new / v_new (rotated), not from the
+ *   cache, and no other request may list the slot.  A mismatch sets
+ *   PA_DEVERR_SLOT (the row is still written at loc[b]; attention then reads
+ *   the table's slot from the cache).
+ *   k_buf, v_buf: written at [layer_id, loc[b]]; the other rows are read.
  * Everything else, the workspace and the limits are those of
  * pa_paged_decode_attn.  A position outside [0, max_pos) sets PA_DEVERR_POS
  * and leaves that token's q and k unrotated, as pa_rope_packed does. */

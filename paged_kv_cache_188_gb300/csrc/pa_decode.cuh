@@ -45,9 +45,11 @@
 //    the (m, l) pairs, the weights are warp-parallel, further splits follow
 //    in batches of the same size.
 //  * Fused decode step (FUSED = true, pa_decode_step): q is rotated (RoPE)
-//    in registers as it is loaded, and the CTA holding the last split of a
-//    (request, kv head) writes that head's new K (rotated) and V rows at
-//    loc[b] before it loads any tile; it is the only CTA that reads them.
+//    in registers as it is loaded.  The warp that computes the last tile of
+//    a (request, kv head)'s last split loads that head's new K and V rows
+//    with q, writes them at loc[b] (K rotated) and puts them over the newest
+//    token's row of its landed tile, so no CTA reads them from the cache and
+//    no tile waits for the store.
 //  * fp8 cache (MODE_FP8, pa_paged_decode_attn_fp8): K/V rows are D bytes of
 //    e4m3 with one scale per (layer, kv head).  Rows reach the ring by
 //    cp.async only.  Keys feed f16 MMAs straight from shared memory: lane t4
@@ -117,7 +119,7 @@ struct DecodeArgs {
     uint64_t wait_ns;    // time limit of the ring waits
     float scale_log2;
     // fused decode step (k_new != null): RoPE on q as it is loaded, and the new
-    // token's rotated K and its V written at loc[b] before any tile is read
+    // token's rotated K and its V written at loc[b] and into the newest tile
     const __nv_bfloat16 *k_new;
     const __nv_bfloat16 *v_new;
     const int32_t *positions;
@@ -342,7 +344,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     __shared__ int s_red[kDecWarps];
     __shared__ int s_flag, s_pend[3];
     __shared__ int s_abort_storage;
-    __shared__ int s_step_n;
     __shared__ int32_t s_pos[FUSED ? kDecThreads : 1];   // fused step: positions[b] of this CTA's first items
     volatile int *s_abort = &s_abort_storage;
 
@@ -533,69 +534,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
 
     // the plan and the first page-table entries only read index arrays; K/V,
     // q, the workspace and out wait for the preceding kernel
-    // Fused step, part 1 (index reads only, so ahead of the wait in
-    // early-metadata mode): every thread examines one of this CTA's items;
-    // the last split of each (request, kv head) -- the only item that reads
-    // the new token -- goes on a list in the scratch (request, kv head, slot,
-    // position).  Part 2, after the wait: groups of 2*D/8 lanes write those
-    // rows (K rotated, V as is), an async-proxy fence and the CTA barrier
-    // order them before this CTA's own TMA / cp.async reads.
-    constexpr int STEP_GROUP = 2 * (D / 8);                 // lanes per row pair (16-byte chunks of K and V)
-    int4 *s_list = reinterpret_cast<int4 *>(scratch);
-    static_assert(L::kScratch >= kDecThreads * (int)sizeof(int4), "step list fits the scratch");
-    int step_err = 0;
-    auto collect = [&](int pass) -> bool {   // whole CTA; false once the CTA has no more items
-        if (tid == 0) s_step_n = 0;
-        __syncthreads();
-        const int first = blockIdx.x + pass * kDecThreads * (int)gridDim.x;
-        const int item = first + tid * (int)gridDim.x;
-        if (item < total_items) {
-            const DecItem I = dec_item<MODE>(a, s_pref, chunk, item);
-            const int32_t p = __ldg(a.positions + I.b);
-            if (pass == 0) s_pos[tid] = p;   // the q rotation of item tid needs no global load later
-            if (I.s == I.sb - 1) {
-                const int32_t slot = __ldg(a.loc + I.b);
-                if (p < 0 || p >= a.max_pos) step_err |= PA_DEVERR_POS;
-                if (slot < 0 || slot >= a.size ||
-                    (I.row >= 0 && I.t1 > 0 && __ldg(a.req_to_token + (int64_t)I.row * a.max_ctx + I.t1 - 1) != slot))
-                    step_err |= PA_DEVERR_SLOT;
-                if (slot >= 0 && slot < a.size) s_list[atomicAdd(&s_step_n, 1)] = make_int4(I.b, I.h, slot, p);
-            }
-        }
-        __syncthreads();
-        return first < total_items;
-    };
-    auto store_rows = [&]() {   // whole CTA
-        const int n = s_step_n;
-        const int li = tid % STEP_GROUP;
-        const bool isv = li >= STEP_GROUP / 2;
-        const int c = li - (isv ? STEP_GROUP / 2 : 0);
-        for (int e = tid / STEP_GROUP; e < n; e += kDecThreads / STEP_GROUP) {
-            const int4 E = s_list[e];
-            const int64_t src = ((int64_t)E.x * Hkv + E.y) * D;
-            uint4 x = __ldg(reinterpret_cast<const uint4 *>((isv ? a.v_new : a.k_new) + src) + c);
-            if (!isv && E.w >= 0 && E.w < a.max_pos) {
-                const float4 cs = __ldg(reinterpret_cast<const float4 *>(a.cos_tab + (int64_t)E.w * (D / 2)) + c);
-                const float4 sn = __ldg(reinterpret_cast<const float4 *>(a.sin_tab + (int64_t)E.w * (D / 2)) + c);
-                x = make_uint4(rope_pair_bf16(x.x, cs.x, sn.x), rope_pair_bf16(x.y, cs.y, sn.y),
-                               rope_pair_bf16(x.z, cs.z, sn.z), rope_pair_bf16(x.w, cs.w, sn.w));
-            }
-            __nv_bfloat16 *dst = (isv ? a.v_layer_w : a.k_layer_w) + (int64_t)E.z * slot_stride + (int64_t)E.y * D;
-            reinterpret_cast<uint4 *>(dst)[c] = x;
-        }
-    };
     // early K/V: a warp's first tiles are copied before the wait, stopping at
     // the first tile that holds a request's newest token (the last tile of
-    // its last split), which the preceding kernel or this CTA may write
+    // its last split), which the preceding kernel may write.  The fused step
+    // does not stop there: it replaces that row in shared memory (below).
     int pre = 0;
     if (early_kv) {
-        while (pre < S - 1 && cur.item < total_items && !(cur.I.s == cur.I.sb - 1 && cur.tile == cur.I.ntiles - 1)) {
+        while (pre < S - 1 && cur.item < total_items &&
+               (FUSED || !(cur.I.s == cur.I.sb - 1 && cur.tile == cur.I.ntiles - 1))) {
             issue();
             ++pre;
         }
     }
-    bool more_steps = false;
-    if (FUSED) more_steps = collect(0);
+    if (FUSED) {
+        // positions[b] of this CTA's first items (an index array: ahead of the
+        // wait in early-metadata mode), so the q rotation needs no global load
+        const int item = blockIdx.x + tid * (int)gridDim.x;
+        if (item < total_items) s_pos[tid] = __ldg(a.positions + item_request(s_pref, a.batch, item));
+        __syncthreads();
+    }
     if (early) pdl_wait();
     pdl_launch_dependents();
     if (MODE == MODE_PREFIX && blockIdx.x == 0) {
@@ -619,16 +576,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 a.req_pre[b] = (lo * a.cpg + i / a.C) * 16 + i % a.C;
             }
         }
-    }
-    if (FUSED) {
-        for (int pass = 1; more_steps; ++pass) {
-            store_rows();
-            __syncthreads();   // list reuse
-            more_steps = collect(pass);
-        }
-        if (step_err) set_error(a.err, step_err);
-        fence_proxy_async_global();
-        __syncthreads();
     }
     for (; pre < S - 1; ++pre) issue();
 
@@ -776,6 +723,60 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             set_error(a.err, PA_DEVERR_TIMEOUT);
             bad = true;
         }
+        // Fused step: the warp that computes the last tile of a (request, kv
+        // head)'s last split -- warp 0 if the item has no tile -- loads that
+        // head's new K and V rows together with q (lane c < D/8: K chunk c;
+        // lane D/8 + c: V chunk c; K lanes also their cos / sin values).  It
+        // writes them at loc[b] (K rotated) and, once the tile has landed,
+        // over the newest token's row of the tile, so the rows are never read
+        // back from the cache.
+        int32_t new_pos = 0, new_slot = -1;
+        bool new_own = false, new_tile = false;
+        uint4 new_x = make_uint4(0u, 0u, 0u, 0u);
+        float4 new_c = make_float4(0.f, 0.f, 0.f, 0.f), new_s = new_c;
+        constexpr int NCH = D / 8;   // 16-byte chunks of a K or V row
+        if constexpr (FUSED) {
+            const int k_item = (item - (int)blockIdx.x) / (int)gridDim.x;
+            new_pos = k_item < kDecThreads ? s_pos[k_item] : __ldg(a.positions + I.b);
+            new_own = I.s == I.sb - 1 && warp == (I.ntiles > 0 ? (I.ntiles - 1) % kDecWarps : 0);
+            if (new_own) {
+                new_slot = __ldg(a.loc + I.b);
+                const bool slot_ok = new_slot >= 0 && new_slot < a.size;
+                const bool pos_ok = new_pos >= 0 && new_pos < a.max_pos;
+                const bool match = I.row >= 0 && I.t1 > 0 &&
+                                   __ldg(a.req_to_token + (int64_t)I.row * a.max_ctx + I.t1 - 1) == new_slot;
+                new_tile = I.ntiles > 0 && slot_ok && match;
+                if (!slot_ok) new_slot = -1;
+                const int e = (pos_ok ? 0 : PA_DEVERR_POS) |
+                              (!slot_ok || (I.row >= 0 && I.t1 > 0 && !match) ? PA_DEVERR_SLOT : 0);
+                if (lane == 0 && e) set_error(a.err, e);
+                const bool isv = lane >= NCH;
+                const int c = lane - (isv ? NCH : 0);
+                if (lane < 2 * NCH) {
+                    const int64_t src = ((int64_t)I.b * Hkv + I.h) * D;
+                    new_x = __ldg(reinterpret_cast<const uint4 *>((isv ? a.v_new : a.k_new) + src) + c);
+                    if (!isv && pos_ok) {
+                        new_c = __ldg(reinterpret_cast<const float4 *>(a.cos_tab + (int64_t)new_pos * (D / 2)) + c);
+                        new_s = __ldg(reinterpret_cast<const float4 *>(a.sin_tab + (int64_t)new_pos * (D / 2)) + c);
+                    }
+                }
+            }
+        }
+        // the new rows as stored (K rotated), written at loc[b]; true if the
+        // tile may take them too
+        auto put_new_rows = [&]() -> uint4 {
+            uint4 x = new_x;
+            if (lane < NCH && new_pos >= 0 && new_pos < a.max_pos)
+                x = make_uint4(rope_pair_bf16(x.x, new_c.x, new_s.x), rope_pair_bf16(x.y, new_c.y, new_s.y),
+                               rope_pair_bf16(x.z, new_c.z, new_s.z), rope_pair_bf16(x.w, new_c.w, new_s.w));
+            if (lane < 2 * NCH && new_slot >= 0) {
+                const bool isv = lane >= NCH;
+                __nv_bfloat16 *dst = (isv ? a.v_layer_w : a.k_layer_w) + (int64_t)new_slot * slot_stride + (int64_t)I.h * D;
+                reinterpret_cast<uint4 *>(dst)[lane - (isv ? NCH : 0)] = x;
+            }
+            return x;
+        };
+        if (FUSED && new_own && I.ntiles == 0) put_new_rows();
         // Q^T as the MMA's B operand: n = head (8 per n-tile), k = d
         uint32_t qb[KSTEPS][NH][2];
         {
@@ -841,8 +842,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 }
             }
             if (FUSED) {
-                const int k_item = (item - (int)blockIdx.x) / (int)gridDim.x;
-                const int32_t p = k_item < kDecThreads ? s_pos[k_item] : __ldg(a.positions + I.b);
+                const int32_t p = new_pos;
                 const int32_t pc = (p >= 0 && p < a.max_pos) ? p : 0;   // out of range: no rotation (below)
                 const float *ct = a.cos_tab + (int64_t)pc * (D / 2), *sn = a.sin_tab + (int64_t)pc * (D / 2);
                 float cv[KSTEPS][2], sv[KSTEPS][2];
@@ -882,6 +882,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 bad = true;
             if (!bad) ++n_landed;
             ++n_done;
+            if (FUSED && new_own && i == I.ntiles - 1) {
+                const uint4 x = put_new_rows();
+                if (!bad && new_tile) {
+                    // the newest token's row of the landed tile: generic writes,
+                    // ordered before the ring's next async-proxy (TMA) refill
+                    const int r = I.t1 - 1 - (I.t0 + i * kDecTile);
+                    if (lane < 2 * NCH) {
+                        const bool isv = lane >= NCH;
+                        const uint32_t tb = ring + st * L::kStage + (isv ? L::kTile : 0);
+                        st_shared_v4(tb + L::off(r, lane - (isv ? NCH : 0)), x.x, x.y, x.z, x.w);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+            }
             if (bad) continue;
             const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile;
             const uint32_t vmask = s_vmask[warp * S + st];

@@ -69,6 +69,31 @@ def test_fused_step_bit_identical_to_three_calls(hq, hkv, d, page):
     assert torch.equal(st.q, q0) and torch.equal(st.k_new, k0)                      # inputs only read
 
 
+def test_fused_step_largest_batch_bit_identical_to_three_calls():
+    # 4096 requests x 16 kv heads, one split each: 65536 items, more than 256
+    # per CTA, so items past a CTA's first 256 read their position from global
+    # memory; every item's new rows go through its own tile
+    B, hq, hkv, d = 4096, 16, 16, 64
+    rng = np.random.default_rng(8)
+    lens = [int(x) for x in rng.integers(1, 41, size=B)]
+    st = _state(lens, hq, hkv, d, 16, seed=8, size=B * 48)
+    ws = api.alloc_workspace(api.pa_decode_workspace_bytes(B, hq, hkv, d, MAX_SPLITS))
+    kb0, vb0 = st.kv.k_buf.clone(), st.kv.v_buf.clone()
+    ref = torch.full_like(st.q, float("nan"))
+    _chain(st, ws, ref)
+    torch.cuda.synchronize()
+    kb_ref, vb_ref = st.kv.k_buf.clone(), st.kv.v_buf.clone()
+    st.kv.k_buf.copy_(kb0)
+    st.kv.v_buf.copy_(vb0)
+    got = torch.full_like(st.q, float("nan"))
+    _step(st, ws, got)
+    torch.cuda.synchronize()
+    assert api.pa_get_error(ws) == 0
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(st.kv.k_buf.view(torch.int16), kb_ref.view(torch.int16))
+    assert torch.equal(st.kv.v_buf.view(torch.int16), vb_ref.view(torch.int16))
+
+
 def test_fused_step_against_oracle_and_graph_replay():
     lens = [2500, 33, 900, 1]
     st = _state(lens, 32, 8, 128, 16, seed=77)
