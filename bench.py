@@ -57,7 +57,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, valid only while the kernel source is unchanged (sha256 prefix).
-NCU_TRAFFIC = {"decode": {"sha": "e7c9c88148619c78", "ratio": round((537.564672 + 2.963712) / 537.460768, 5),
+NCU_TRAFFIC = {"decode": {"sha": "17521fbd836893d3", "ratio": round((537.542656 + 2.984192) / 537.460768, 5),
                           "capture": "ncu, 4 x 32K tokens, one layer: dram read+write 540.53 MB for "
                                      "537.46 MB algorithmic; scaled to this workload by algorithmic bytes"}}
 
@@ -71,7 +71,8 @@ def parse():
     p.add_argument("--only-main", action="store_true", help="skip the secondary workloads")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--no-fp8", action="store_true", help="skip the sweep over an e4m3 copy of the cache")
-    p.add_argument("--profile", choices=["decode", "decode_shared_prefix", "prefill", "prefill_fp8", "rope", "store"],
+    p.add_argument("--profile", choices=["decode", "decode_shared_prefix", "decode_page1", "prefill", "prefill_fp8",
+                                             "rope", "store"],
                    default=None,
                    help="run a small fixed case of one kernel (for ncu captures) and exit")
     return p.parse_args()
@@ -780,6 +781,23 @@ def run_profile_case(args):
         unique = (st.kv.used_slots.numel() + B) * HKV * D * 4
         print(json.dumps({"profile": "decode_shared_prefix", "launches": 3,
                           "logical_kv_bytes": sum(lens) * HKV * D * 4, "unique_kv_bytes": unique,
+                          "device_error_word": api.pa_get_error(ws)}))
+    elif args.profile == "decode_page1":
+        # the first 128 requests of the B=256 token-granular batch (Hq=64, log-normal
+        # lengths, page size 1) over a 512K-slot buffer: 2 GiB of K/V, one layer
+        lens = W.config5_lens()[:128]
+        st = W.make_decode_step(lens=lens, n_q_heads=64, n_kv_heads=HKV, head_dim=D, n_layers=1,
+                                size=1 << 19, page_size=1, seed=5, max_ctx=32768, device=dev)
+        api.pa_kv_store(st.kv.k_buf, st.kv.v_buf, 0, st.k_new, st.v_new, st.loc)
+        B = len(lens)
+        ws = api.alloc_workspace(api.pa_decode_workspace_bytes(B, 64, HKV, D, MAX_SPLITS), dev)
+        out = torch.empty_like(st.q)
+        for _ in range(3):
+            api.pa_paged_decode_attn(st.q, st.kv.k_buf, st.kv.v_buf, 0, st.kv.req_to_token, st.kv.req_pool_indices,
+                                     st.kv.seq_lens, st.scale, ws, MAX_SPLITS, out, stream=s)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "decode_page1", "launches": 3,
+                          "algorithmic_bytes_per_launch": sum(decode_bytes(n, Hq=64) for n in lens),
                           "device_error_word": api.pa_get_error(ws)}))
     elif args.profile == "prefill":
         pb = W.config4(device=dev)
