@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_HERE, "libpagedattn.so")
 PA_OK = 0
 STATUS = {0: "PA_OK", 1: "PA_ERR_NULL", 2: "PA_ERR_SHAPE", 3: "PA_ERR_ALIGN", 4: "PA_ERR_UNSUPPORTED",
           5: "PA_ERR_WORKSPACE", 6: "PA_ERR_CUDA", 7: "PA_ERR_DEVICE_INDEX"}
-DEVERR_SLOT, DEVERR_ROW, DEVERR_LEN, DEVERR_POS = 0x1, 0x2, 0x4, 0x8
+DEVERR_SLOT, DEVERR_ROW, DEVERR_LEN, DEVERR_POS, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
 OVERLAP_OFF, OVERLAP_SAFE, OVERLAP_EARLY_METADATA, OVERLAP_EARLY_KV = 0, 1, 2, 3
 
 

@@ -34,6 +34,19 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // Wait until every cp.async this thread issued has landed.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
+// L2 load of *p if `pred` (else 0), kept in program order with the other
+// memory operations (volatile, memory clobber): a batch of these is issued
+// where it is written, not moved down to the first use of its values.
+__device__ __forceinline__ float ld_cg_ordered_if(bool pred, const float *p)
+{
+    float v = 0.f;
+    asm volatile("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.cg.f32 %0, [%1];\n}\n"
+                 : "+f"(v)
+                 : "l"(p), "r"((int)pred)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"

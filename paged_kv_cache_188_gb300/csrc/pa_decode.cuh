@@ -634,22 +634,29 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 const int e = tid + k * kDecThreads;
 #pragma unroll
                 for (int j = 0; j < SB; ++j)
-                    v[k][j] = (e < G * D && ss + j < sb) ? __ldcg(obase + e + (ss + j) * split_stride) : 0.f;
+                    v[k][j] = ld_cg_ordered_if(e < G * D && ss + j < sb, obase + e + (ss + j) * split_stride);
             }
         };
-        load_batch(0);
+        // this warp's first head's (m, l) pairs, then the first batch of
+        // partials: all requested before any value is used (one round trip)
         const int64_t ml_stride = (int64_t)a.cap_batch * a.Hq * 2;   // floats per split
-        for (int gg = warp; gg < G; gg += kDecWarps) {
+        float mv[SPL], lv[SPL];
+        auto load_ml = [&](int gg) {
             const float *ml = a.ml_part + ((int64_t)b * a.Hq + hq0 + gg) * 2;
-            float mv[SPL], lv[SPL];
-            float M = -INFINITY;
 #pragma unroll
             for (int r = 0; r < SPL; ++r) {
                 const int ss = lane + 32 * r;
                 mv[r] = ss < sb ? __ldcg(ml + ss * ml_stride) : -INFINITY;
                 lv[r] = ss < sb ? __ldcg(ml + ss * ml_stride + 1) : 0.f;
-                M = fmaxf(M, mv[r]);
             }
+        };
+        if (warp < G) load_ml(warp);
+        load_batch(0);
+        for (int gg = warp; gg < G; gg += kDecWarps) {
+            if (gg != warp) load_ml(gg);
+            float M = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < SPL; ++r) M = fmaxf(M, mv[r]);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
             const float Mr = M == -INFINITY ? 0.f : M;
