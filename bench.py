@@ -57,7 +57,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture, valid only while the kernel source is unchanged (sha256 prefix).
-NCU_TRAFFIC = {"decode": {"sha": "17521fbd836893d3", "ratio": round((537.542656 + 2.984192) / 537.460768, 5),
+NCU_TRAFFIC = {"decode": {"sha": "dd2cda6e0bd15d79", "ratio": round((537.540608 + 2.976768) / 537.460768, 5),
                           "capture": "ncu, 4 x 32K tokens, one layer: dram read+write 540.53 MB for "
                                      "537.46 MB algorithmic; scaled to this workload by algorithmic bytes"}}
 
@@ -419,9 +419,14 @@ def run_ours(args, rank, world, local):
                           "frac_of_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)})
     g_rope = capture(lambda: sw.step(("rope",)), s)
     g_store = capture(lambda: sw.step(("store",)), s)
+    # plain decode alone in the step's own graph shape (all 192 layer-calls),
+    # the baseline of the fused step's extra cost
+    g_dec_step = capture(lambda: sw.step(("decode",)), s)
     n_calls = N_LAYERS * len(SWEEP)
     rope_us = time_graph(g_rope, reps, s) / n_calls * 1e3
     store_us = time_graph(g_store, reps, s) / n_calls * 1e3
+    g_dec_step.replay()
+    dec_step_ms = time_graph(g_dec_step, reps, s)
     dec_gbs = dec_bytes_tot / (dec_ms_tot * 1e-3) / 1e9
     traffic = NCU_TRAFFIC.get("decode")
     traffic_val = None
@@ -466,7 +471,9 @@ def run_ours(args, rank, world, local):
         "gpu_launches_per_step": sw.launches_per_step,
         "frac_of_hbm_peak": round(value / peaks["hbm_gbs"], 4),
         "decode": {"per_context": per_point, "gbs": round(dec_gbs, 1),
-                   "rope_us_per_call": round(rope_us, 3), "kv_store_us_per_call": round(store_us, 3)},
+                   "rope_us_per_call": round(rope_us, 3), "kv_store_us_per_call": round(store_us, 3),
+                   "decode_only_ms_per_step": round(dec_step_ms, 4),
+                   "fused_extra_us_per_call": round((ms_step - dec_step_ms) / n_calls * 1e3, 3)},
         "roofline": {"kernel": "paged_decode_kernel<D=128,S=3,NH=1>", "bound": "hbm", "achieved": round(dec_gbs, 1),
                      "peak": peaks["hbm_gbs"], "peak_source": peak_src, "unit": "GB/s",
                      "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "traffic": traffic_val,
