@@ -52,6 +52,7 @@ from paged_kv_cache_188_gb300 import workloads as W  # noqa: E402
 
 SWEEP = [1024, 2048, 4096, 8192, 16384, 32768]
 N_LAYERS, SIZE, HQ, HKV, D, PAGE = 32, 65536, 32, 8, 128, 16
+L2_BYTES = 129 * 1024 * 1024   # GB300 L2
 MAX_SPLITS = 64
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -417,6 +418,27 @@ def run_ours(args, rank, world, local):
         per_point.append({"seq_len": n, "us_per_layer": round(ms * 1e3, 3),
                           "gbs": round(b / (ms * 1e-3) / 1e9, 1),
                           "frac_of_hbm": round(b / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)})
+    # a second figure: layer 17 alone, a write of 2.5x the L2 size between
+    # calls (so every call starts with its K/V out of L2), minus a graph of
+    # the writes alone
+    scratch = torch.empty(int(2.5 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    n_cold = 8
+
+    def cold_calls(p=None):
+        for _ in range(n_cold):
+            if p is not None:
+                sw.layer_call(p, 17, ("decode",))
+            scratch.zero_()
+    g_scr = capture(cold_calls, s)
+    g_scr.replay()
+    ms_scr = time_graph(g_scr, reps, s)
+    cold_us = []
+    for p, n in enumerate(SWEEP):
+        g = capture(lambda: cold_calls(p), s)
+        g.replay()
+        cold_us.append(round((time_graph(g, reps, s) - ms_scr) / n_cold * 1e3, 3))
+        del g
+    del scratch, g_scr
     g_rope = capture(lambda: sw.step(("rope",)), s)
     g_store = capture(lambda: sw.step(("store",)), s)
     # plain decode alone in the step's own graph shape (all 192 layer-calls),
@@ -473,6 +495,7 @@ def run_ours(args, rank, world, local):
         "decode": {"per_context": per_point, "gbs": round(dec_gbs, 1),
                    "rope_us_per_call": round(rope_us, 3), "kv_store_us_per_call": round(store_us, 3),
                    "decode_only_ms_per_step": round(dec_step_ms, 4),
+                   "layer17_cold_l2_us_per_context": cold_us,
                    "fused_extra_us_per_call": round((ms_step - dec_step_ms) / n_calls * 1e3, 3)},
         "roofline": {"kernel": "paged_decode_kernel<D=128,S=3,NH=1>", "bound": "hbm", "achieved": round(dec_gbs, 1),
                      "peak": peaks["hbm_gbs"], "peak_source": peak_src, "unit": "GB/s",

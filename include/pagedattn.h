@@ -208,7 +208,12 @@ pa_status pa_rope_packed(void *q, int n_q_heads, void *k, int n_kv_heads, int he
  * Computed as split-KV flash-decoding: each (request, kv head) range is cut
  * into at most max_splits pieces, chosen on the device from seq_lens and the
  * SM count, whose fp32 partials (o_part, ml_part) are merged by log-sum-exp in
- * a fixed order (run-to-run bit-identical).
+ * a fixed order (run-to-run bit-identical).  With at most half as many
+ * (request, kv head) pairs as SMs, the merge runs inside the one decode
+ * kernel (the CTA that completes a pair merges it).  A larger batch is two
+ * kernels on `st`: decode, which writes every split's partials, then a merge
+ * kernel spread over the whole GPU (it writes only out).  This also holds for
+ * pa_decode_step and pa_paged_decode_attn_fp8.
  * Supported: head_dim in {64, 128}; 1 <= G <= 16; 1 <= max_splits <= 128;
  * batch <= 4096 and <= the workspace's cap_batch for these head counts and
  * max_splits.  A 16-token tile whose positions sit on one page moves as TMA

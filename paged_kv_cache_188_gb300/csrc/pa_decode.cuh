@@ -116,6 +116,8 @@ struct DecodeArgs {
     int layer_row0;      // layer_id * size: tensor-map row of slot 0 of the layer
     int early_meta;      // launched behind another kernel: plan and page table before waiting for it
     int early_kv;        // ... and copy K/V tiles (not the requests' newest rows) before waiting for it
+    int defer_merge;     // large batch: every split's partials written, merged by a second kernel (no tickets)
+    int plan_grid;       // CTAs of the decode launch (the plan the deferred merge recomputes)
     uint64_t wait_ns;    // time limit of the ring waits
     float scale_log2;
     // fused decode step (k_new != null): RoPE on q as it is loaded, and the new
@@ -158,6 +160,20 @@ struct DecPlan {
     int budget;
     float inv_tot;   // budget / total tokens (every CTA computes the same value)
 };
+
+// The plan of a launch of `grid` CTAs over B requests of `tot` tokens in all
+// (every CTA, and the deferred merge, computes the same values).
+__device__ __forceinline__ DecPlan make_plan(long long tot, int B, int Hkv, int grid)
+{
+    const long long want = (tot * Hkv + grid - 1) / grid;
+    DecPlan p;
+    p.chunk = (int)((want + kDecMinChunk - 1) / kDecMinChunk * kDecMinChunk);
+    p.chunk = p.chunk < kDecMinChunk ? kDecMinChunk : (p.chunk > kDecMaxChunk ? kDecMaxChunk : p.chunk);
+    // one wave for small batches whose common split length would hit the cap
+    p.budget = (2 * B * Hkv <= grid && want > kDecMaxChunk) ? grid / Hkv : 0;
+    p.inv_tot = p.budget > 0 ? (float)p.budget / (float)tot : 0.f;
+    return p;
+}
 
 // split count and split length (tokens) of a request of n tokens
 __device__ __forceinline__ void split_of(int n, const DecPlan &pl, int max_splits, int &sb, int &len)
@@ -369,13 +385,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     long long tot = 0;
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) tot += s_red[w];
-    const long long want = (tot * Hkv + gridDim.x - 1) / gridDim.x;
-    DecPlan chunk;
-    chunk.chunk = (int)((want + kDecMinChunk - 1) / kDecMinChunk * kDecMinChunk);
-    chunk.chunk = chunk.chunk < kDecMinChunk ? kDecMinChunk : (chunk.chunk > kDecMaxChunk ? kDecMaxChunk : chunk.chunk);
-    // one wave for small batches whose common split length would hit the cap
-    chunk.budget = (2 * B * Hkv <= (int)gridDim.x && want > kDecMaxChunk) ? (int)gridDim.x / Hkv : 0;
-    chunk.inv_tot = chunk.budget > 0 ? (float)chunk.budget / (float)tot : 0.f;
+    const DecPlan chunk = make_plan(tot, B, Hkv, (int)gridDim.x);
     {
         const int per = (B + kDecThreads - 1) / kDecThreads;
         const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
@@ -1164,7 +1174,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 }
             }
         }
-        if (I.sb > 1) {
+        if (I.sb > 1 && !a.defer_merge) {
             // ticket for (b, h): the barrier orders every thread's partial
             // stores before thread 0's acquire-release atomic (release: this
             // CTA's partials; acquire: those of the CTAs that came before, for
@@ -1190,6 +1200,91 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     if (ring_err) set_error(a.err, ring_err);
 }
 
+// Deferred split merge of a large batch.  The decode kernel wrote every
+// split's partials and merged nothing: with many items per CTA, the CTA that
+// completed a (request, kv head) last would merge it, and the merges piled up
+// on the CTAs that were already behind.  This kernel merges every (request,
+// kv head) of more than one split, one per CTA at a time, over the whole GPU,
+// after the decode kernel (it waits for it first).  It recomputes the decode
+// launch's plan (plan_grid CTAs), so it sees the same split counts, and does
+// the in-kernel merge's arithmetic: split weights warp-parallel, each element
+// summed in split order.
+template <int D, int NH>
+__global__ void __launch_bounds__(kDecThreads) paged_decode_merge_kernel(const __grid_constant__ DecodeArgs a)
+{
+    constexpr int GMAX = 8 * NH;
+    constexpr int EPT = (GMAX * D + kDecThreads - 1) / kDecThreads;
+    constexpr int SPL = kDecMaxSplits / 32;   // splits per lane
+    __shared__ float s_w[kDecMaxSplits * GMAX];   // [split][head] weights
+    __shared__ float s_lt[GMAX];                  // weighted sums of l
+    __shared__ long long s_red[kDecWarps];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = a.batch, Hkv = a.Hkv, G = a.G;
+    pdl_wait();
+    pdl_launch_dependents();
+    long long my_tot = 0;
+    for (int b = tid; b < B; b += kDecThreads) my_tot += clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) my_tot += __shfl_xor_sync(0xffffffffu, my_tot, o);
+    if (lane == 0) s_red[warp] = my_tot;
+    __syncthreads();
+    long long tot = 0;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) tot += s_red[w];
+    const DecPlan plan = make_plan(tot, B, Hkv, a.plan_grid);
+    const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
+    const int64_t ml_stride = (int64_t)a.cap_batch * a.Hq * 2;
+    for (int p = blockIdx.x; p < B * Hkv; p += gridDim.x) {
+        const int b = p / Hkv, h = p - b * Hkv;
+        int sb, len;
+        split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), plan, a.max_splits, sb, len);
+        if (sb <= 1) continue;   // written by the decode kernel
+        const int hq0 = h * G;
+        for (int gg = warp; gg < G; gg += kDecWarps) {
+            const float *ml = a.ml_part + ((int64_t)b * a.Hq + hq0 + gg) * 2;
+            float mv[SPL], lv[SPL];
+            float M = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < SPL; ++r) {
+                const int ss = lane + 32 * r;
+                mv[r] = ss < sb ? __ldcg(ml + ss * ml_stride) : -INFINITY;
+                lv[r] = ss < sb ? __ldcg(ml + ss * ml_stride + 1) : 0.f;
+                M = fmaxf(M, mv[r]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            const float Mr = M == -INFINITY ? 0.f : M;
+            float lt = 0.f;
+#pragma unroll
+            for (int r = 0; r < SPL; ++r) {
+                const int ss = lane + 32 * r;
+                if (ss < sb) {
+                    const float wt = ex2(mv[r] - Mr);
+                    s_w[ss * G + gg] = wt;
+                    lt += wt * lv[r];
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+            if (lane == 0) s_lt[gg] = lt;
+        }
+        __syncthreads();
+        const float *obase = a.o_part + ((int64_t)b * a.Hq + hq0) * D;
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int e = tid + k * kDecThreads;
+            if (e >= G * D) continue;
+            const int gg = e / D;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int ss = 0; ss < sb; ++ss) acc += s_w[ss * G + gg] * __ldcg(obase + e + ss * split_stride);
+            const float lt = s_lt[gg];
+            a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
+        }
+        __syncthreads();   // s_w, s_lt reuse
+    }
+}
+
 template <int D, int S, int NH, int MODE>
 static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
 {
@@ -1198,6 +1293,14 @@ static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
     if (smem > kSmemLimit) return PA_ERR_UNSUPPORTED;
     if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kern), smem)) return PA_ERR_CUDA;
     if (launch_kernel(kern, dim3(num_sms()), dim3(kDecThreads), smem, st, a) != cudaSuccess) return PA_ERR_CUDA;
+    if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8) {
+        if (a.defer_merge) {
+            const int pairs = a.batch * a.Hkv, cap = 8 * num_sms();
+            if (launch_kernel(paged_decode_merge_kernel<D, NH>, dim3(pairs < cap ? pairs : cap), dim3(kDecThreads), 0,
+                              st, a) != cudaSuccess)
+                return PA_ERR_CUDA;
+        }
+    }
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -1314,8 +1417,15 @@ static bool fill_decode_args(DecodeArgs &a, const void *q, int batch, int n_q_he
 }
 
 template <int MODE>
-static pa_status dispatch_mode(const DecodeArgs &a, int head_dim, cudaStream_t st)
+static pa_status dispatch_mode(const DecodeArgs &a0, int head_dim, cudaStream_t st)
 {
+    DecodeArgs a = a0;
+    if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8) {
+        // more (request, kv head) pairs than half the CTAs: many items per CTA,
+        // merged by the second kernel
+        a.plan_grid = num_sms();
+        a.defer_merge = 2 * a.batch * a.Hkv > a.plan_grid;
+    }
     if (head_dim == 128) return a.G > 8 ? dispatch_decode<128, 2, MODE>(a, st) : dispatch_decode<128, 1, MODE>(a, st);
     return a.G > 8 ? dispatch_decode<64, 2, MODE>(a, st) : dispatch_decode<64, 1, MODE>(a, st);
 }

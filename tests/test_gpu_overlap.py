@@ -6,6 +6,7 @@ overlap off, safe, early-metadata and early-KV, eagerly and under repeated graph
 replay.  Early-KV mode copies cache rows other than each request's newest
 one before the wait, which these chains allow (the store writes only the
 newest rows)."""
+import numpy as np
 import pytest
 import torch
 
@@ -41,14 +42,20 @@ def _decode_chain(st, q0, k0, ws, outs, stream):
                                  st.kv.seq_lens, st.scale, ws, 64, out, stream=stream)
 
 
-def _decode_state():
-    st = W.make_decode_step(lens=[3000, 17, 1200, 640], n_q_heads=32, n_kv_heads=8, head_dim=128, n_layers=2,
-                            size=16384, page_size=16, seed=31, layer=1, max_ctx=4096, device="cuda")
+# 24 requests x 8 kv heads: more pairs than half the CTAs, so each decode
+# call is the decode kernel and the deferred-merge kernel
+LARGE = [int(x) for x in np.random.default_rng(24).integers(1, 4000, size=24)]
+
+
+def _decode_state(lens=(3000, 17, 1200, 640)):
+    st = W.make_decode_step(lens=list(lens), n_q_heads=32, n_kv_heads=8, head_dim=128, n_layers=2,
+                            size=131072, page_size=16, seed=31, layer=1, max_ctx=4096, device="cuda")
     return st, st.q.clone(), st.k_new.clone()
 
 
-def test_decode_chain_identical_across_modes_eager_and_graph():
-    st, q0, k0 = _decode_state()
+@pytest.mark.parametrize("lens", [(3000, 17, 1200, 640), tuple(LARGE)], ids=["small", "large"])
+def test_decode_chain_identical_across_modes_eager_and_graph(lens):
+    st, q0, k0 = _decode_state(lens)
     B, Hq, D = st.q.shape
     ws = api.alloc_workspace(api.pa_decode_workspace_bytes(B, Hq, 8, D, 64))
     ref = None
