@@ -229,7 +229,9 @@ struct DecSmem {
     static constexpr int kMaskOff = kScratchOff + kScratch;
     static constexpr int kBarOff = kMaskOff + kDecWarps * S * 4;
     static constexpr int kPrefOff = kBarOff + kDecWarps * S * 8;
-    static constexpr size_t bytes(int batch) { return 1024 + (size_t)kPrefOff + (size_t)(batch + 1) * 4; }
+    // after the prefix array [batch + 1]: each request's (clamped length, table row), int2 [batch]
+    __host__ __device__ static constexpr size_t req_off(int batch) { return (size_t)kPrefOff + (size_t)(batch + 2) / 2 * 8; }
+    static constexpr size_t bytes(int batch) { return 1024 + req_off(batch) + (size_t)batch * 8; }
     // byte offset of 16-byte chunk c of row r inside a K or V tile
     __device__ static __forceinline__ uint32_t off(int r, int c)
     {
@@ -300,8 +302,11 @@ __device__ __forceinline__ int req_len(const DecodeArgs &a, int b)
     }
 }
 
+// s_req (plain, fused and fp8 modes): each request's clamped length and
+// table row, read from global memory once, during the plan.
 template <int MODE>
-__device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pref, const DecPlan &chunk, int item)
+__device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pref, const int2 *s_req,
+                                            const DecPlan &chunk, int item)
 {
     const int lo = item_request(s_pref, a.batch, item);
     DecItem I;
@@ -310,10 +315,11 @@ __device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pr
     I.s = local / a.Hkv;
     I.h = local - I.s * a.Hkv;
     if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8) {
-        int n = clamp_len(__ldg(a.seq_lens + lo), a.max_ctx);
+        const int2 rq = s_req[lo];
+        int n = rq.x;
         int len;
         split_of(n, chunk, a.max_splits, I.sb, len);
-        I.row = __ldg(a.req_pool_indices + lo);
+        I.row = rq.y;
         if (I.row < 0 || I.row >= a.req_rows) {
             I.row = -1;
             n = 0;
@@ -356,6 +362,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     float *scratch = reinterpret_cast<float *>(smem + L::kScratchOff);
     uint32_t *s_vmask = reinterpret_cast<uint32_t *>(smem + L::kMaskOff);
     int32_t *s_pref = reinterpret_cast<int32_t *>(smem + L::kPrefOff);
+    int2 *s_req = reinterpret_cast<int2 *>(smem + L::req_off(a.batch));
     __shared__ float s_m[kDecWarps][16], s_l[kDecWarps][16];
     __shared__ int s_red[kDecWarps];
     __shared__ int s_flag, s_pend[3];
@@ -409,9 +416,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         int excl = base + incl - run;
         for (int b = b_lo; b < b_hi; ++b) {
             s_pref[b] = excl;
+            const int n = req_len<MODE>(a, b);
             int sb, len;
-            split_of(req_len<MODE>(a, b), chunk, a.max_splits, sb, len);
+            split_of(n, chunk, a.max_splits, sb, len);
             excl += sb * Hkv;
+            if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8)
+                s_req[b] = make_int2(n, __ldg(a.req_pool_indices + b));
         }
         if (tid == kDecThreads - 1) s_pref[B] = base + incl;
     }
@@ -435,7 +445,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         while (c.item < total_items && c.tile >= c.I.ntiles) {
             c.item += gridDim.x;
             c.tile = warp;
-            if (c.item < total_items) c.I = dec_item<MODE>(a, s_pref, chunk, c.item);
+            if (c.item < total_items) c.I = dec_item<MODE>(a, s_pref, s_req, chunk, c.item);
         }
         c.slot = -1;
         if (c.item < total_items && lane < kDecTile && c.I.row >= 0) {
@@ -449,7 +459,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     cur.I.ntiles = 0;
     cur.I.row = -1;
     cur.I.t0 = cur.I.t1 = cur.I.h = 0;
-    if (cur.item < total_items) cur.I = dec_item<MODE>(a, s_pref, chunk, cur.item);
+    if (cur.item < total_items) cur.I = dec_item<MODE>(a, s_pref, s_req, chunk, cur.item);
     // the CTA's first item, kept for the item loop: in early-metadata mode it
     // is derived before the wait, so the loop's first iteration re-reads nothing
     const DecItem first_I = cur.I;
@@ -732,7 +742,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     int n_landed = 0; // tiles whose ring wait succeeded: those after it may still be in flight
     bool ticket_pending = false;   // CTA-uniform: the previous item took a merge ticket
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const DecItem I = item == (int)blockIdx.x ? first_I : dec_item<MODE>(a, s_pref, chunk, item);
+        const DecItem I = item == (int)blockIdx.x ? first_I : dec_item<MODE>(a, s_pref, s_req, chunk, item);
         const int hq0 = I.h * G;
         if (a.wait_ns == 0 && !bad) {
             // a wait limit of 0: give up at the first item, as a timed-out ring wait would
