@@ -154,6 +154,23 @@ def test_batch_changes_within_one_workspace():
     assert api.pa_get_error(ws) == 0
 
 
+def test_claimed_items_with_idle_warps_match_oracle():
+    # a large batch (items claimed from the workspace counter) of tiny
+    # requests: most items have fewer tiles than warps, so most warps skip
+    # many items in a row; the whole output against the oracle, twice
+    B = 1024
+    lens = [int(x) for x in np.random.default_rng(17).integers(1, 61, size=B)]
+    st = W.make_decode_step(lens=lens, n_q_heads=16, n_kv_heads=8, head_dim=64, n_layers=1, size=B * 64,
+                            page_size=16, seed=17, max_ctx=64, device="cuda")
+    kb, vb = _store_raw(st)
+    ref = _oracle_full(st, kb, vb)
+    ws = _ws(B, 16, 8, 64)
+    for _ in range(2):
+        out, _ = _decode(st, ws=ws)
+        assert_attention_close(npy(out.float()), ref, "claimed items, idle warps")
+    assert api.pa_get_error(ws) == 0
+
+
 def test_bad_slot_sets_error_and_is_skipped():
     st = W.make_decode_step(lens=[40, 40], n_q_heads=8, n_kv_heads=2, head_dim=64, n_layers=1, size=256,
                             page_size=16, seed=8, device="cuda")
