@@ -154,9 +154,9 @@ def test_batch_changes_within_one_workspace():
     assert api.pa_get_error(ws) == 0
 
 
-def test_claimed_items_with_idle_warps_match_oracle():
-    # a large batch (items claimed from the workspace counter) of tiny
-    # requests: most items have fewer tiles than warps, so most warps skip
+def test_large_batch_of_tiny_requests_matches_oracle():
+    # a large batch (many items per CTA, deferred merge) of tiny requests:
+    # most items have fewer tiles than warps, so most warps' load cursors skip
     # many items in a row; the whole output against the oracle, twice
     B = 1024
     lens = [int(x) for x in np.random.default_rng(17).integers(1, 61, size=B)]
@@ -167,7 +167,7 @@ def test_claimed_items_with_idle_warps_match_oracle():
     ws = _ws(B, 16, 8, 64)
     for _ in range(2):
         out, _ = _decode(st, ws=ws)
-        assert_attention_close(npy(out.float()), ref, "claimed items, idle warps")
+        assert_attention_close(npy(out.float()), ref, "tiny requests, idle warps")
     assert api.pa_get_error(ws) == 0
 
 
