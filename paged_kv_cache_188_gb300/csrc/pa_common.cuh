@@ -34,6 +34,19 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // Wait until every cp.async this thread issued has landed.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
+// Read-only load of *p if `pred` (else -1), kept in program order with the
+// other memory operations (volatile, memory clobber): issued where it is
+// written, not moved down to the first use of its value.
+__device__ __forceinline__ int32_t ld_nc_ordered_s32_if(bool pred, const int32_t *p)
+{
+    int32_t v = -1;
+    asm volatile("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.nc.s32 %0, [%1];\n}\n"
+                 : "+r"(v)
+                 : "l"(p), "r"((int)pred)
+                 : "memory");
+    return v;
+}
+
 // L2 load of *p if `pred` (else 0), kept in program order with the other
 // memory operations (volatile, memory clobber): a batch of these is issued
 // where it is written, not moved down to the first use of its values.

@@ -353,9 +353,24 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
             const int row0 = DENSE ? I.qs : p.layer_row0;
             const int col0 = I.h * D;
             const int gi = lane >> 2, sub = lane & 3;
+            // page-table entries of positions 128 t + 4 lane + e: the next
+            // tile's are requested while this one's copies are issued, so a
+            // tile's K copy waits for no table round trip (after the item's
+            // first tile)
+            int nraw[4];
+            auto load_raw = [&](int tt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int pos = tt * kPfKeys + 4 * lane + e;
+                    nraw[e] = DENSE ? pos : ld_nc_ordered_s32_if(pos < I.n_keys, r2t + pos);
+                }
+            };
+            if (I.ntiles > 0) load_raw(0);
             for (int t = 0; t < I.ntiles; ++t, ++kt) {
                 const int st = kt & 1;
                 const uint32_t ph_prev = ((kt >> 1) - 1) & 1;
+                const int raw[4] = {nraw[0], nraw[1], nraw[2], nraw[3]};
+                if (t + 1 < I.ntiles) load_raw(t + 1);
                 // slots of positions k0 + 4*lane + e
                 const int k0 = t * kPfKeys;
                 int slot[4];
@@ -364,7 +379,7 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
                 for (int e = 0; e < 4; ++e) {
                     const int pos = k0 + 4 * lane + e;
                     okp[e] = pos < I.n_keys;
-                    slot[e] = okp[e] ? (DENSE ? pos : __ldg(r2t + pos)) : -1;
+                    slot[e] = okp[e] ? raw[e] : -1;
                     if (okp[e] && !DENSE && (slot[e] < 0 || slot[e] >= p.size)) {   // skipped: zeros, flagged
                         set_error(err, PA_DEVERR_SLOT);
                         okp[e] = false;
