@@ -7,7 +7,7 @@
 // request r (position p_r + i, p_r = cached prefix) attends to positions
 // 0 .. p_r + i of the request, K/V rows read through req_to_token.
 //
-// How (persistent, one CTA per SM, warp-specialised, 320 threads):
+// How (persistent, one CTA per SM, warp-specialised, 352 threads):
 //  * Work item = (request, pair of q tiles, kv head).  A q tile packs the G
 //    query heads of one kv head into the MMA's M = 128 rows: 128/G
 //    consecutive tokens x G heads (token-major).  The two tiles A and B of a
@@ -15,8 +15,10 @@
 //  * Items are claimed from a counter in the workspace (heaviest pairs of a
 //    request first), so CTAs that drew short items take more of them; the
 //    producer hands each claim to the other roles through a small ring.
-//  * warp 8 (producer): TMA.  Q tiles via a 3-D tensor map (d, head, token);
-//    K/V tiles of 128 positions gathered through req_to_token: a group of 16
+//  * warps 8 and 10 (producers): TMA; warp 8 claims the items and loads Q
+//    and K, warp 10 loads V (fp8: warp 8 loads all three).  Q tiles via a
+//    3-D tensor map (d, head, token); K/V tiles of 128 positions gathered
+//    through req_to_token (the next tile's entries requested ahead): a group of 16
 //    positions on 16 consecutive slots (one page) is one 16-row box per 64-wide
 //    half, anything else falls back to 1-row boxes; positions past the pair's
 //    last visible key load zeros (out-of-range rows).  128-byte swizzle, the
@@ -49,9 +51,10 @@ using namespace sm100;
 
 constexpr int kPfRows = 128;            // MMA M: rows of a q tile
 constexpr int kPfKeys = 128;            // keys per kv tile
-constexpr int kPfThreads = 320;         // 8 softmax warps + producer + MMA issuer
+constexpr int kPfThreads = 352;         // 8 softmax warps + K producer + MMA issuer + V producer
 constexpr int kPfThreadsF8 = 384;       // e4m3 cache: + two warps widening K / V tiles to bf16
 constexpr int kWarpProducer = 8, kWarpMma = 9, kWarpCvtK = 10, kWarpCvtV = 11;
+constexpr int kWarpProducerV = 10;      // bf16 kernels: V tiles are issued by a warp of their own
 constexpr int kPfMaxReqs = 2048;
 constexpr int kHalf = 128 * 128;        // one 128-row x 128-byte swizzled half tile (16 KB): 64 of D columns
 constexpr int kRing = 4;               // claimed work items handed from the producer to the other roles
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
         for (int i = 0; i < N_BARS; ++i) {
             const bool softmax_arrive = i == PA_FULL || i == PB_FULL || i == OA_EMPTY || i == OB_EMPTY;
             const bool item_read = i >= ITEM_EMPTY && i < ITEM_EMPTY + kRing;
-            mbar_init(bar(i), softmax_arrive ? 128u : item_read ? (uint32_t)(kItemReaders + (F8 ? 2 : 0)) : 1u);
+            mbar_init(bar(i), softmax_arrive ? 128u : item_read ? (uint32_t)(kItemReaders + (F8 ? 2 : 1)) : 1u);
         }
         fence_mbar_init();
     }
@@ -307,11 +310,18 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
     const int total_items = s_pref[p.R];
     const int G = p.G;
 
-    if (warp == kWarpProducer) {
-        // ================================================== TMA producer
+    if (warp == kWarpProducer || (!F8 && warp == kWarpProducerV)) {
+        // ================================================== TMA producers
         // Items are claimed one at a time from a global counter, so a CTA that
         // drew short items takes more of them; each claim (and finally the
         // first index past the end) goes to the other roles through a ring.
+        // bf16: warp 8 claims items and loads Q and the K tiles, warp 10 reads
+        // the ring and loads the V tiles, so the two tiles' copies are issued
+        // in parallel (each 16-row box is a TMA instruction of its own, and
+        // one warp issuing both tiles had become the step's critical path).
+        // fp8: warp 8 loads everything.
+        const bool doK = warp == kWarpProducer;
+        const bool doV = F8 || warp == kWarpProducerV;
         int kt = 0;
         int nq = 0, nk = 0, nv = 0;   // Q, K and V loads armed (for the drain on abort)
         bool ok = true;
@@ -321,25 +331,33 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
         };
         for (int it = 0; ok; ++it) {
             const int slot = it % kRing;
-            if (it >= kRing && !wait1(ITEM_EMPTY + slot, (it / kRing - 1) & 1)) break;
-            int item = 0;
-            if (lane == 0) item = atomicAdd(p.queue, 1);
-            item = __shfl_sync(0xffffffffu, item, 0);
             PfItem I;
-            if (item < total_items) {
-                I = pf_item<DENSE>(p, s_pref, item);
-                I.end = 0;
+            if (doK) {
+                if (it >= kRing && !wait1(ITEM_EMPTY + slot, (it / kRing - 1) & 1)) break;
+                int item = 0;
+                if (lane == 0) item = atomicAdd(p.queue, 1);
+                item = __shfl_sync(0xffffffffu, item, 0);
+                if (item < total_items) {
+                    I = pf_item<DENSE>(p, s_pref, item);
+                    I.end = 0;
+                } else {
+                    I.end = 1;
+                }
+                if (lane == 0) {
+                    s_ring[slot] = I;
+                    mbar_arrive(bar(ITEM_FULL + slot));
+                }
             } else {
-                I.end = 1;
-            }
-            if (lane == 0) {
-                s_ring[slot] = I;
-                mbar_arrive(bar(ITEM_FULL + slot));
+                // the V producer reads the claim like the other roles
+                if (!wait1(ITEM_FULL + slot, (it / kRing) & 1)) break;
+                I = s_ring[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(ITEM_EMPTY + slot));
             }
             if (I.end) break;
-            if (it > 0 && !wait1(Q_EMPTY, (it - 1) & 1)) break;
-            ++nq;
-            if (lane == 0) {
+            if (doK && it > 0 && !wait1(Q_EMPTY, (it - 1) & 1)) break;
+            if (doK) ++nq;
+            if (doK && lane == 0) {
                 mbar_arrive_expect_tx(bar(Q_FULL), 2 * QH * kHalf);
 #pragma unroll
                 for (int hh = 0; hh < QH; ++hh) {
@@ -455,33 +473,38 @@ __global__ void __launch_bounds__(F8 ? kPfThreadsF8 : kPfThreads, 1)
                         }
                     }
                 };
-                if (kt >= 2 && !wait1(K_EMPTY + st, ph_prev)) {
-                    ok = false;
-                    break;
+                if (doK) {
+                    if (kt >= 2 && !wait1(K_EMPTY + st, ph_prev)) {
+                        ok = false;
+                        break;
+                    }
+                    if (any_gathered) {
+                        gather(p.k_rows, sK + st * QH * kHalf);
+                        cp_async_wait_all();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    ++nk;
+                    if (lane == 0) mbar_arrive_expect_tx(bar(kb + st), tile_bytes);
+                    __syncwarp();
+                    issue(&p.tm_k16, &p.tm_k1, F8 ? raw_tile(false, st) : sK + st * QH * kHalf, bar(kb + st));
                 }
-                if (any_gathered) {
+                if (doV) {
                     if (kt >= 2 && !wait1(V_EMPTY + st, ph_prev)) {
                         ok = false;
                         break;
                     }
-                    gather(p.k_rows, sK + st * QH * kHalf);
-                    gather(p.v_rows, sV + st * QH * kHalf);
-                    cp_async_wait_all();
-                    fence_proxy_async_smem();
+                    if (any_gathered) {
+                        gather(p.v_rows, sV + st * QH * kHalf);
+                        cp_async_wait_all();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    ++nv;
+                    if (lane == 0) mbar_arrive_expect_tx(bar(vb + st), tile_bytes);
                     __syncwarp();
+                    issue(&p.tm_v16, &p.tm_v1, F8 ? raw_tile(true, st) : sV + st * QH * kHalf, bar(vb + st));
                 }
-                ++nk;
-                if (lane == 0) mbar_arrive_expect_tx(bar(kb + st), tile_bytes);
-                __syncwarp();
-                issue(&p.tm_k16, &p.tm_k1, F8 ? raw_tile(false, st) : sK + st * QH * kHalf, bar(kb + st));
-                if (!any_gathered && kt >= 2 && !wait1(V_EMPTY + st, ph_prev)) {
-                    ok = false;
-                    break;
-                }
-                ++nv;
-                if (lane == 0) mbar_arrive_expect_tx(bar(vb + st), tile_bytes);
-                __syncwarp();
-                issue(&p.tm_v16, &p.tm_v1, F8 ? raw_tile(true, st) : sV + st * QH * kHalf, bar(vb + st));
             }
         }
         if (*s_abort && lane == 0) {
