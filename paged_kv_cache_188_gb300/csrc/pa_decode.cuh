@@ -13,8 +13,8 @@
 // How (one kernel, one persistent CTA of 8 warps per SM):
 //  * Planning on the device, redundantly in every CTA: sum of seq_lens ->
 //    per request the split count s_b (<= max_splits): splits of a common
-//    length (at most 1024 tokens), or -- when batch x Hkv is at most half the
-//    grid and that length would pass 1024 -- counts proportional to the
+//    length (at most 2048 tokens), or -- when batch x Hkv is at most half the
+//    grid and that length would pass 2048 -- counts proportional to the
 //    lengths that fill the grid in one wave; a prefix sum over s_b * Hkv
 //    enumerates work items (b, split, kv head).  The grid never depends on
 //    device lengths, so a captured graph stays valid.
@@ -76,7 +76,7 @@ constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecTile = 16;        // tokens per ring stage
 constexpr int kDecMinChunk = 64;    // split length bounds (tokens)
-constexpr int kDecMaxChunk = 1024;
+constexpr int kDecMaxChunk = 2048;
 constexpr int kDecMaxBatch = 4096;
 constexpr int kDecMaxSplits = 128;
 
@@ -228,7 +228,11 @@ struct DecSmem {
     static constexpr int kScratch = kCombine > kMerge ? kCombine : kMerge;
     static constexpr int kMaskOff = kScratchOff + kScratch;
     static constexpr int kBarOff = kMaskOff + kDecWarps * S * 4;
-    static constexpr int kPrefOff = kBarOff + kDecWarps * S * 8;
+    // q rows of the current item [8 NH][D / 2 + 4] words (bf16 pairs; rows
+    // padded so the fragment reads, 8 rows x 4 words, hit distinct banks)
+    static constexpr int kQStride = D / 2 + 4;
+    static constexpr int kQOff = kBarOff + kDecWarps * S * 8;
+    static constexpr int kPrefOff = kQOff + 8 * NH * kQStride * 4;
     // after the prefix array [batch + 1]: each request's (clamped length, table row), int2 [batch]
     __host__ __device__ static constexpr size_t req_off(int batch) { return (size_t)kPrefOff + (size_t)(batch + 2) / 2 * 8; }
     static constexpr size_t bytes(int batch) { return 1024 + req_off(batch) + (size_t)batch * 8; }
@@ -808,11 +812,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         uint32_t qb[KSTEPS][NH][2];
         {
             const uint32_t *q32 = reinterpret_cast<const uint32_t *>(a.q + ((int64_t)I.b * a.Hq + hq0) * D);
-            // every load is issued before any use: q words first, then (fused
-            // step) the cos/sin values of this lane's pairs -- word i of a head
-            // row is RoPE pair i, rotated by table row positions[b]
-            // (prefix launch: row hd of a virtual request is head hd % G of
-            // member hd / G of its chunk, G the real GQA group)
+            // every load is issued before any use; word i of a head row is
+            // RoPE pair i (fused step: rotated by table row positions[b]);
+            // prefix launch: row hd of a virtual request is head hd % G of
+            // member hd / G of its chunk, G the real GQA group
             if constexpr (F8) {
                 // the keys' permuted head dimension: k-step kk of lane t4
                 // covers d = t4 * D/4 + 4 kk + {0, 1 | 2, 3}; q as f16
@@ -833,13 +836,43 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                         qb[kk][nt][1] = bf16x2_to_f16x2_sat(qb[kk][nt][1]);
                     }
             } else if constexpr (MODE != MODE_PREFIX) {
+                // the item's G head rows through shared memory: every thread
+                // loads whole words of them (consecutive threads, consecutive
+                // words), the fused step rotates each pair once per CTA, and
+                // every warp then reads its B fragments from the staged rows
+                uint32_t *s_q = reinterpret_cast<uint32_t *>(smem + L::kQOff);
+                constexpr int QW = D / 2;   // words (RoPE pairs) of a head row
+                constexpr int QE = (8 * NH * QW + kDecThreads - 1) / kDecThreads;
+                int32_t pc = 0;
+                bool rot = false;
+                if constexpr (FUSED) {
+                    pc = (new_pos >= 0 && new_pos < a.max_pos) ? new_pos : 0;   // out of range: no rotation
+                    rot = pc == new_pos;
+                }
+                uint32_t qw[QE];
+                float qc[QE], qs[QE];
+#pragma unroll
+                for (int k = 0; k < QE; ++k) {
+                    const int e = tid + k * kDecThreads, hd = e / QW, i = e - hd * QW;
+                    qw[k] = hd < G ? __ldg(q32 + hd * QW + i) : 0u;
+                    if constexpr (FUSED) {
+                        qc[k] = hd < G ? __ldg(a.cos_tab + (int64_t)pc * QW + i) : 0.f;
+                        qs[k] = hd < G ? __ldg(a.sin_tab + (int64_t)pc * QW + i) : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < QE; ++k) {
+                    const int e = tid + k * kDecThreads, hd = e / QW, i = e - hd * QW;
+                    if (hd < 8 * NH) s_q[hd * L::kQStride + i] = (FUSED && rot) ? rope_pair_bf16(qw[k], qc[k], qs[k]) : qw[k];
+                }
+                __syncthreads();
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk)
 #pragma unroll
                     for (int nt = 0; nt < NH; ++nt) {
-                        const int hd = nt * 8 + g;
-                        qb[kk][nt][0] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + t4) : 0u;
-                        qb[kk][nt][1] = hd < G ? __ldg(q32 + hd * (D / 2) + kk * 8 + 4 + t4) : 0u;
+                        const uint32_t *row = s_q + (nt * 8 + g) * L::kQStride + kk * 8 + t4;
+                        qb[kk][nt][0] = row[0];
+                        qb[kk][nt][1] = row[4];
                     }
             } else {
             const uint32_t *qrow[NH];
@@ -866,28 +899,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 for (int nt = 0; nt < NH; ++nt) {
                     qb[kk][nt][0] = qok[nt] ? __ldg(qrow[nt] + kk * 8 + t4) : 0u;
                     qb[kk][nt][1] = qok[nt] ? __ldg(qrow[nt] + kk * 8 + 4 + t4) : 0u;
-                }
-            }
-            if (FUSED) {
-                const int32_t p = new_pos;
-                const int32_t pc = (p >= 0 && p < a.max_pos) ? p : 0;   // out of range: no rotation (below)
-                const float *ct = a.cos_tab + (int64_t)pc * (D / 2), *sn = a.sin_tab + (int64_t)pc * (D / 2);
-                float cv[KSTEPS][2], sv[KSTEPS][2];
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS; ++kk) {
-                    cv[kk][0] = __ldg(ct + kk * 8 + t4);
-                    cv[kk][1] = __ldg(ct + kk * 8 + 4 + t4);
-                    sv[kk][0] = __ldg(sn + kk * 8 + t4);
-                    sv[kk][1] = __ldg(sn + kk * 8 + 4 + t4);
-                }
-                if (pc == p) {
-#pragma unroll
-                    for (int kk = 0; kk < KSTEPS; ++kk)
-#pragma unroll
-                        for (int nt = 0; nt < NH; ++nt) {
-                            qb[kk][nt][0] = rope_pair_bf16(qb[kk][nt][0], cv[kk][0], sv[kk][0]);
-                            qb[kk][nt][1] = rope_pair_bf16(qb[kk][nt][1], cv[kk][1], sv[kk][1]);
-                        }
                 }
             }
         }

@@ -87,7 +87,7 @@ def test_ragged_batch(Hq, Hkv, D, page):
 @pytest.mark.parametrize("max_splits", [1, 2, 3, 8, 64, 128])
 def test_split_count_invariance(max_splits):
     """Any split cap gives the oracle's result; caps below the planned count
-    stretch splits beyond one staged index window (1024 tokens)."""
+    stretch splits beyond the plan's longest split (2048 tokens)."""
     lens = [5000, 3, 2048, 777]
     st = W.make_decode_step(lens=lens, n_q_heads=32, n_kv_heads=8, head_dim=128, n_layers=1, size=16384,
                             page_size=16, seed=123, req_rows=4, max_ctx=5000, device="cuda")
