@@ -816,26 +816,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
             // RoPE pair i (fused step: rotated by table row positions[b]);
             // prefix launch: row hd of a virtual request is head hd % G of
             // member hd / G of its chunk, G the real GQA group
-            if constexpr (F8) {
-                // the keys' permuted head dimension: k-step kk of lane t4
-                // covers d = t4 * D/4 + 4 kk + {0, 1 | 2, 3}; q as f16
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS; ++kk)
-#pragma unroll
-                    for (int nt = 0; nt < NH; ++nt) {
-                        const int hd = nt * 8 + g;
-                        const int w = t4 * (D / 8) + 2 * kk;
-                        qb[kk][nt][0] = hd < G ? __ldg(q32 + hd * (D / 2) + w) : 0u;
-                        qb[kk][nt][1] = hd < G ? __ldg(q32 + hd * (D / 2) + w + 1) : 0u;
-                    }
-#pragma unroll
-                for (int kk = 0; kk < KSTEPS; ++kk)
-#pragma unroll
-                    for (int nt = 0; nt < NH; ++nt) {
-                        qb[kk][nt][0] = bf16x2_to_f16x2_sat(qb[kk][nt][0]);
-                        qb[kk][nt][1] = bf16x2_to_f16x2_sat(qb[kk][nt][1]);
-                    }
-            } else if constexpr (MODE != MODE_PREFIX) {
+            if constexpr (MODE != MODE_PREFIX) {
                 // the item's G head rows through shared memory: every thread
                 // loads whole words of them (consecutive threads, consecutive
                 // words), the fused step rotates each pair once per CTA, and
@@ -863,16 +844,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
 #pragma unroll
                 for (int k = 0; k < QE; ++k) {
                     const int e = tid + k * kDecThreads, hd = e / QW, i = e - hd * QW;
-                    if (hd < 8 * NH) s_q[hd * L::kQStride + i] = (FUSED && rot) ? rope_pair_bf16(qw[k], qc[k], qs[k]) : qw[k];
+                    uint32_t x = (FUSED && rot) ? rope_pair_bf16(qw[k], qc[k], qs[k]) : qw[k];
+                    if constexpr (F8) x = bf16x2_to_f16x2_sat(x);   // fp8 cache: q as f16
+                    if (hd < 8 * NH) s_q[hd * L::kQStride + i] = x;
                 }
                 __syncthreads();
 #pragma unroll
                 for (int kk = 0; kk < KSTEPS; ++kk)
 #pragma unroll
                     for (int nt = 0; nt < NH; ++nt) {
-                        const uint32_t *row = s_q + (nt * 8 + g) * L::kQStride + kk * 8 + t4;
-                        qb[kk][nt][0] = row[0];
-                        qb[kk][nt][1] = row[4];
+                        if constexpr (F8) {
+                            // the keys' permuted head dimension: k-step kk of
+                            // lane t4 covers d = t4 D/4 + 4 kk + {0, 1 | 2, 3}
+                            const uint32_t *row = s_q + (nt * 8 + g) * L::kQStride + t4 * (D / 8) + 2 * kk;
+                            qb[kk][nt][0] = row[0];
+                            qb[kk][nt][1] = row[1];
+                        } else {
+                            const uint32_t *row = s_q + (nt * 8 + g) * L::kQStride + kk * 8 + t4;
+                            qb[kk][nt][0] = row[0];
+                            qb[kk][nt][1] = row[4];
+                        }
                     }
             } else {
             const uint32_t *qrow[NH];
