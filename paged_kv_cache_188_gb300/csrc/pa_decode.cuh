@@ -159,11 +159,25 @@ struct DecPlan {
     int chunk;
     int budget;
     float inv_tot;   // budget / total tokens (every CTA computes the same value)
+    int bal;         // balanced large-batch plan (below)
+    int W;           // bal: tiles per CTA
 };
+
+// Balanced plan for large batches whose merges are deferred: the (kv head,
+// request) segments, head-major, are laid end to end as 16-token tiles (at
+// least one per segment, so an empty request still writes its zero output),
+// and CTA c takes tiles [c W, (c + 1) W).  Each piece of a segment inside one
+// CTA's range is an item; a segment's pieces are its splits, in CTA order.
+// Every CTA then streams the same number of tiles, whatever the mix of
+// lengths (round-robin items of a common length left CTAs up to 15 % above
+// the mean), and one CTA reads consecutive requests of one kv head, so pages
+// that requests share are read again while they are in L2.
+__device__ __forceinline__ int seg_tiles(int n) { return n > 0 ? (n + kDecTile - 1) / kDecTile : 1; }
 
 // The plan of a launch of `grid` CTAs over B requests of `tot` tokens in all
 // (every CTA, and the deferred merge, computes the same values).
-__device__ __forceinline__ DecPlan make_plan(long long tot, int B, int Hkv, int grid)
+__device__ __forceinline__ DecPlan make_plan(long long tot, int B, int Hkv, int grid, long long tiles = 0,
+                                             int tb_max = 0, int max_splits = 0, bool allow_bal = false)
 {
     const long long want = (tot * Hkv + grid - 1) / grid;
     DecPlan p;
@@ -172,6 +186,18 @@ __device__ __forceinline__ DecPlan make_plan(long long tot, int B, int Hkv, int 
     // one wave for small batches whose common split length would hit the cap
     p.budget = (2 * B * Hkv <= grid && want > kDecMaxChunk) ? grid / Hkv : 0;
     p.inv_tot = p.budget > 0 ? (float)p.budget / (float)tot : 0.f;
+    // balanced: W tiles per CTA, a multiple of the warp count; a segment of
+    // tb tiles has at most ceil(tb / W) + 1 pieces, which must fit max_splits
+    p.bal = 0;
+    p.W = 0;
+    const long long T = tiles * Hkv;
+    if (allow_bal && 2 * B * Hkv > grid && T < (1LL << 30)) {
+        const long long W = ((T + grid - 1) / grid + kDecWarps - 1) / kDecWarps * kDecWarps;
+        if ((tb_max + W - 1) / W + 1 <= max_splits) {
+            p.bal = 1;
+            p.W = (int)W;
+        }
+    }
     return p;
 }
 
@@ -253,7 +279,8 @@ constexpr size_t kSmemLimit = 232448 - 4096;   // opt-in maximum minus static sh
 // Everything an item needs, derived from the plan (identical in every warp).
 struct DecItem {
     int b, s, h, sb, t0, t1, ntiles;
-    int row;   // -1 if the request row is invalid
+    int row;    // -1 if the request row is invalid
+    int wofs;   // tile i of the item is computed by warp (i + wofs) % 8
 };
 
 // request of a work item: the largest b with s_pref[b] <= item (shared memory only)
@@ -310,10 +337,38 @@ __device__ __forceinline__ int req_len(const DecodeArgs &a, int b)
 // table row, read from global memory once, during the plan.
 template <int MODE>
 __device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pref, const int2 *s_req,
-                                            const DecPlan &chunk, int item)
+                                            const DecPlan &chunk, int item, int seg0 = 0)
 {
-    const int lo = item_request(s_pref, a.batch, item);
     DecItem I;
+    I.wofs = 0;
+    if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8) {
+        if (chunk.bal) {
+            // piece p of this CTA's tile range: segment seg0 + p (s_pref holds
+            // each request's first tile within a kv head's run of segments)
+            const int seg = seg0 + (item - (int)blockIdx.x) / (int)gridDim.x;
+            I.h = seg / a.batch;
+            I.b = seg - I.h * a.batch;
+            const int2 rq = s_req[I.b];
+            int n = rq.x;
+            const int tb = seg_tiles(n);
+            const int S0 = I.h * s_pref[a.batch] + s_pref[I.b];   // the segment's first tile
+            const int x0 = (int)blockIdx.x * chunk.W;
+            const int u0 = max(x0, S0), u1 = min(x0 + chunk.W, S0 + tb);
+            I.s = (int)blockIdx.x - S0 / chunk.W;
+            I.sb = (S0 + tb - 1) / chunk.W - S0 / chunk.W + 1;
+            I.row = rq.y;
+            if (I.row < 0 || I.row >= a.req_rows) {
+                I.row = -1;
+                n = 0;
+            }
+            I.t0 = (u0 - S0) * kDecTile;
+            I.t1 = min(n, (u1 - S0) * kDecTile);
+            I.ntiles = I.t1 > I.t0 ? (I.t1 - I.t0 + kDecTile - 1) / kDecTile : 0;
+            I.wofs = (u0 - x0) & (kDecWarps - 1);
+            return I;
+        }
+    }
+    const int lo = item_request(s_pref, a.batch, item);
     I.b = lo;
     const int local = item - s_pref[lo];
     I.s = local / a.Hkv;
@@ -346,7 +401,9 @@ __device__ __forceinline__ DecItem dec_item(const DecodeArgs &a, const int *s_pr
     return I;
 }
 
-template <int D, int S, int NH, int MODE>
+// BAL: the instance for large batches (merges deferred), which takes the
+// balanced plan when it fits; the other instances carry none of its code.
+template <int D, int S, int NH, int MODE, bool BAL = false>
 __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __grid_constant__ DecodeArgs a)
 {
     using L = DecSmem<D, S, NH, MODE == MODE_FP8>;
@@ -368,7 +425,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     int32_t *s_pref = reinterpret_cast<int32_t *>(smem + L::kPrefOff);
     int2 *s_req = reinterpret_cast<int2 *>(smem + L::req_off(a.batch));
     __shared__ float s_m[kDecWarps][16], s_l[kDecWarps][16];
-    __shared__ int s_red[kDecWarps];
+    __shared__ int s_red[kDecWarps], s_red2[kDecWarps], s_red3[kDecWarps];
     __shared__ int s_flag, s_pend[3];
     __shared__ int s_abort_storage;
     __shared__ int32_t s_pos[FUSED ? kDecThreads : 1];   // fused step: positions[b] of this CTA's first items
@@ -387,25 +444,55 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     if (!early) pdl_wait();
 
     // ---------------------------------------------------------- planning
-    int my_tot = 0;
-    for (int b = tid; b < B; b += kDecThreads) my_tot += req_len<MODE>(a, b);
+    // the balanced plan: large batches of the plain, fused and fp8 modes,
+    // whose merges the second kernel does
+    constexpr bool kBal = BAL && (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8);
+    int my_tot = 0, my_tiles = 0, my_tbmax = 0;
+    for (int b = tid; b < B; b += kDecThreads) {
+        const int n = req_len<MODE>(a, b);
+        my_tot += n;
+        if constexpr (kBal) {
+            my_tiles += seg_tiles(n);
+            my_tbmax = max(my_tbmax, seg_tiles(n));
+        }
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) my_tot += __shfl_xor_sync(0xffffffffu, my_tot, o);
-    if (lane == 0) s_red[warp] = my_tot;
+    for (int o = 16; o > 0; o >>= 1) {
+        my_tot += __shfl_xor_sync(0xffffffffu, my_tot, o);
+        if constexpr (kBal) {
+            my_tiles += __shfl_xor_sync(0xffffffffu, my_tiles, o);
+            my_tbmax = max(my_tbmax, __shfl_xor_sync(0xffffffffu, my_tbmax, o));
+        }
+    }
+    if (lane == 0) {
+        s_red[warp] = my_tot;
+        s_red2[warp] = my_tiles;
+        s_red3[warp] = my_tbmax;
+    }
     __syncthreads();
-    long long tot = 0;
+    long long tot = 0, tiles = 0;
+    int tb_max = 0;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) tot += s_red[w];
-    const DecPlan chunk = make_plan(tot, B, Hkv, (int)gridDim.x);
+    for (int w = 0; w < kDecWarps; ++w) {
+        tot += s_red[w];
+        if constexpr (kBal) {
+            tiles += s_red2[w];
+            tb_max = max(tb_max, s_red3[w]);
+        }
+    }
+    const DecPlan chunk = make_plan(tot, B, Hkv, (int)gridDim.x, tiles, tb_max, a.max_splits, kBal && a.defer_merge);
     {
         const int per = (B + kDecThreads - 1) / kDecThreads;
         const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
-        int run = 0;
-        for (int b = b_lo; b < b_hi; ++b) {
+        // items (split x kv head) per request, or (balanced) its tiles
+        auto units = [&](int n) -> int {
+            if (chunk.bal) return seg_tiles(n);   // per kv head
             int sb, len;
-            split_of(req_len<MODE>(a, b), chunk, a.max_splits, sb, len);
-            run += sb * Hkv;
-        }
+            split_of(n, chunk, a.max_splits, sb, len);
+            return sb * Hkv;
+        };
+        int run = 0;
+        for (int b = b_lo; b < b_hi; ++b) run += units(req_len<MODE>(a, b));
         int incl = run;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -421,9 +508,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         for (int b = b_lo; b < b_hi; ++b) {
             s_pref[b] = excl;
             const int n = req_len<MODE>(a, b);
-            int sb, len;
-            split_of(n, chunk, a.max_splits, sb, len);
-            excl += sb * Hkv;
+            excl += units(n);
             if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8)
                 s_req[b] = make_int2(n, __ldg(a.req_pool_indices + b));
         }
@@ -431,6 +516,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     }
     __syncthreads();
     const int total_items = s_pref[B];
+    // this CTA's items are blockIdx.x, + gridDim.x, ... below item_end; in the
+    // balanced plan, piece p of its tile range (segments seg0, seg0 + 1, ...)
+    int item_end = total_items, seg0 = 0;
+    if (chunk.bal) {
+        // total_items: the tiles of one kv head's segments
+        const int x0 = (int)blockIdx.x * chunk.W, T = Hkv * total_items;
+        item_end = 0;
+        if (x0 < T) {
+            const int xl = min(x0 + chunk.W, T) - 1;
+            const int h0 = x0 / total_items, hl = xl / total_items;
+            seg0 = h0 * B + item_request(s_pref, B, x0 - h0 * total_items);
+            const int segl = hl * B + item_request(s_pref, B, xl - hl * total_items);
+            item_end = (int)blockIdx.x + (segl - seg0 + 1) * (int)gridDim.x;
+        }
+    }
     const int64_t slot_stride = (int64_t)Hkv * D;
     const uint32_t ring = smem_u32(smem) + warp * L::kRing;
     bool bad = false;   // a ring wait timed out: skip work, keep the barriers
@@ -446,24 +546,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         DecItem I;
     };
     auto settle = [&](Cursor &c) {
-        while (c.item < total_items && c.tile >= c.I.ntiles) {
+        while (c.item < item_end && c.tile >= c.I.ntiles) {
             c.item += gridDim.x;
-            c.tile = warp;
-            if (c.item < total_items) c.I = dec_item<MODE>(a, s_pref, s_req, chunk, c.item);
+            if (c.item < item_end) c.I = dec_item<MODE>(a, s_pref, s_req, chunk, c.item, seg0);
+            c.tile = (warp - c.I.wofs) & (kDecWarps - 1);
         }
         c.slot = -1;
-        if (c.item < total_items && lane < kDecTile && c.I.row >= 0) {
+        if (c.item < item_end && lane < kDecTile && c.I.row >= 0) {
             const int tok = c.I.t0 + c.tile * kDecTile + lane;
             if (tok < c.I.t1) c.slot = __ldg(a.req_to_token + (int64_t)c.I.row * a.max_ctx + tok);
         }
     };
     Cursor cur;
     cur.item = blockIdx.x;
-    cur.tile = warp;
     cur.I.ntiles = 0;
     cur.I.row = -1;
-    cur.I.t0 = cur.I.t1 = cur.I.h = 0;
-    if (cur.item < total_items) cur.I = dec_item<MODE>(a, s_pref, s_req, chunk, cur.item);
+    cur.I.t0 = cur.I.t1 = cur.I.h = cur.I.wofs = 0;
+    if (cur.item < item_end) cur.I = dec_item<MODE>(a, s_pref, s_req, chunk, cur.item, seg0);
+    cur.tile = (warp - cur.I.wofs) & (kDecWarps - 1);
     // the CTA's first item, kept for the item loop: in early-metadata mode it
     // is derived before the wait, so the loop's first iteration re-reads nothing
     const DecItem first_I = cur.I;
@@ -474,7 +574,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     int n_issued = 0;
     // load the `cur` tile into ring stage n_issued % S, then advance both cursors
     auto issue = [&]() {
-        if (cur.item >= total_items) return;
+        if (cur.item >= item_end) return;
         const int st = n_issued % S;
         const uint32_t kb = ring + st * L::kStage, vb = kb + L::kTile, fb = bars + st * 8;
         const int tok0 = cur.I.t0 + cur.tile * kDecTile;
@@ -564,7 +664,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     // does not stop there: it replaces that row in shared memory (below).
     int pre = 0;
     if (early_kv) {
-        while (pre < S - 1 && cur.item < total_items &&
+        while (pre < S - 1 && cur.item < item_end &&
                (FUSED || !(cur.I.s == cur.I.sb - 1 && cur.tile == cur.I.ntiles - 1))) {
             issue();
             ++pre;
@@ -574,7 +674,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         // positions[b] of this CTA's first items (an index array: ahead of the
         // wait in early-metadata mode), so the q rotation needs no global load
         const int item = blockIdx.x + tid * (int)gridDim.x;
-        if (item < total_items) s_pos[tid] = __ldg(a.positions + item_request(s_pref, a.batch, item));
+        if (item < item_end)
+            s_pos[tid] = __ldg(a.positions + (chunk.bal ? (seg0 + tid) % B : item_request(s_pref, a.batch, item)));
         __syncthreads();
     }
     if (early) pdl_wait();
@@ -745,8 +846,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
     int n_done = 0;   // tiles computed (or, after a timed-out wait, skipped) by this warp
     int n_landed = 0; // tiles whose ring wait succeeded: those after it may still be in flight
     bool ticket_pending = false;   // CTA-uniform: the previous item took a merge ticket
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const DecItem I = item == (int)blockIdx.x ? first_I : dec_item<MODE>(a, s_pref, s_req, chunk, item);
+    for (int item = blockIdx.x; item < item_end; item += gridDim.x) {
+        const DecItem I = item == (int)blockIdx.x ? first_I : dec_item<MODE>(a, s_pref, s_req, chunk, item, seg0);
         const int hq0 = I.h * G;
         if (a.wait_ns == 0 && !bad) {
             // a wait limit of 0: give up at the first item, as a timed-out ring wait would
@@ -769,7 +870,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
         if constexpr (FUSED) {
             const int k_item = (item - (int)blockIdx.x) / (int)gridDim.x;
             new_pos = k_item < kDecThreads ? s_pos[k_item] : __ldg(a.positions + I.b);
-            new_own = I.s == I.sb - 1 && warp == (I.ntiles > 0 ? (I.ntiles - 1) % kDecWarps : 0);
+            new_own = I.s == I.sb - 1 && warp == (I.ntiles > 0 ? (I.ntiles - 1 + I.wofs) % kDecWarps : 0);
             if (new_own) {
                 new_slot = __ldg(a.loc + I.b);
                 const bool slot_ok = new_slot >= 0 && new_slot < a.size;
@@ -904,7 +1005,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
 
         float sl2_f8 = 0.f;   // fp8: softmax scale (log2 units) times the head's K scale
         if constexpr (F8) sl2_f8 = a.scale_log2 * __ldg(a.k_scale + I.h);
-        for (int i = warp; i < I.ntiles; i += kDecWarps) {
+        for (int i = (warp - I.wofs) & (kDecWarps - 1); i < I.ntiles; i += kDecWarps) {
             if (!bad) issue();
             const int st = n_done % S;
             if (!bad && !mbar_wait(bars + st * 8, (n_done / S) & 1, s_abort, a.err, PA_DEVERR_TIMEOUT, a.wait_ns))
@@ -1230,26 +1331,77 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_merge_kernel(const _
     __shared__ float s_w[kDecMaxSplits * GMAX];   // [split][head] weights
     __shared__ float s_lt[GMAX];                  // weighted sums of l
     __shared__ long long s_red[kDecWarps];
+    __shared__ int s_red2[kDecWarps], s_red3[kDecWarps];
+    __shared__ int s_tp[kDecMaxBatch + 1];        // balanced plan: each request's first tile
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.batch, Hkv = a.Hkv, G = a.G;
     pdl_wait();
     pdl_launch_dependents();
     long long my_tot = 0;
-    for (int b = tid; b < B; b += kDecThreads) my_tot += clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
+    int my_tiles = 0, my_tbmax = 0;
+    for (int b = tid; b < B; b += kDecThreads) {
+        const int n = clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
+        my_tot += n;
+        my_tiles += seg_tiles(n);
+        my_tbmax = max(my_tbmax, seg_tiles(n));
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) my_tot += __shfl_xor_sync(0xffffffffu, my_tot, o);
-    if (lane == 0) s_red[warp] = my_tot;
+    for (int o = 16; o > 0; o >>= 1) {
+        my_tot += __shfl_xor_sync(0xffffffffu, my_tot, o);
+        my_tiles += __shfl_xor_sync(0xffffffffu, my_tiles, o);
+        my_tbmax = max(my_tbmax, __shfl_xor_sync(0xffffffffu, my_tbmax, o));
+    }
+    if (lane == 0) {
+        s_red[warp] = my_tot;
+        s_red2[warp] = my_tiles;
+        s_red3[warp] = my_tbmax;
+    }
     __syncthreads();
-    long long tot = 0;
+    long long tot = 0, tiles = 0;
+    int tb_max = 0;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) tot += s_red[w];
-    const DecPlan plan = make_plan(tot, B, Hkv, a.plan_grid);
+    for (int w = 0; w < kDecWarps; ++w) {
+        tot += s_red[w];
+        tiles += s_red2[w];
+        tb_max = max(tb_max, s_red3[w]);
+    }
+    // the decode launch's plan (this kernel runs only for deferred merges)
+    const DecPlan plan = make_plan(tot, B, Hkv, a.plan_grid, tiles, tb_max, a.max_splits, true);
+    if (plan.bal) {
+        // each request's first tile within a kv head's run: an exclusive prefix of its segment tiles
+        const int per = (B + kDecThreads - 1) / kDecThreads;
+        const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
+        int run = 0;
+        for (int b = b_lo; b < b_hi; ++b) run += seg_tiles(clamp_len(__ldg(a.seq_lens + b), a.max_ctx));
+        int incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        __syncthreads();   // s_red2 reuse
+        if (lane == 31) s_red2[warp] = incl;
+        __syncthreads();
+        int excl = incl - run;
+        for (int w = 0; w < warp; ++w) excl += s_red2[w];
+        for (int b = b_lo; b < b_hi; ++b) {
+            s_tp[b] = excl;
+            excl += seg_tiles(clamp_len(__ldg(a.seq_lens + b), a.max_ctx));
+        }
+        __syncthreads();
+    }
     const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
     const int64_t ml_stride = (int64_t)a.cap_batch * a.Hq * 2;
     for (int p = blockIdx.x; p < B * Hkv; p += gridDim.x) {
         const int b = p / Hkv, h = p - b * Hkv;
+        const int n = clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
         int sb, len;
-        split_of(clamp_len(__ldg(a.seq_lens + b), a.max_ctx), plan, a.max_splits, sb, len);
+        if (plan.bal) {
+            const int tb = seg_tiles(n), S0 = h * (int)tiles + s_tp[b];
+            sb = (S0 + tb - 1) / plan.W - S0 / plan.W + 1;
+        } else {
+            split_of(n, plan, a.max_splits, sb, len);
+        }
         if (sb <= 1) continue;   // written by the decode kernel
         const int hq0 = h * G;
         for (int gg = warp; gg < G; gg += kDecWarps) {
@@ -1297,10 +1449,10 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_merge_kernel(const _
     }
 }
 
-template <int D, int S, int NH, int MODE>
+template <int D, int S, int NH, int MODE, bool BAL = false>
 static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
 {
-    auto kern = paged_decode_kernel<D, S, NH, MODE>;
+    auto kern = paged_decode_kernel<D, S, NH, MODE, BAL>;
     const size_t smem = DecSmem<D, S, NH, MODE == MODE_FP8>::bytes(a.batch);
     if (smem > kSmemLimit) return PA_ERR_UNSUPPORTED;
     if (!ensure_dynamic_smem(reinterpret_cast<const void *>(kern), smem)) return PA_ERR_CUDA;
@@ -1320,6 +1472,21 @@ static pa_status launch_decode(const DecodeArgs &a, cudaStream_t st)
 template <int D, int NH, int MODE>
 static pa_status dispatch_decode(const DecodeArgs &a, cudaStream_t st)
 {
+    constexpr bool kCanBal = MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8;
+    if constexpr (kCanBal) {
+        // large batches (merges deferred): the instance with the balanced plan
+        if (a.defer_merge) {
+            if constexpr (MODE == MODE_FP8) {
+                if (DecSmem<D, 5, NH, true>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 5, NH, MODE, true>(a, st);
+                if (DecSmem<D, 4, NH, true>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 4, NH, MODE, true>(a, st);
+                return launch_decode<D, 2, NH, MODE, true>(a, st);
+            } else {
+                if (DecSmem<D, 4, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 4, NH, MODE, true>(a, st);
+                if (DecSmem<D, 3, NH>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 3, NH, MODE, true>(a, st);
+                return launch_decode<D, 2, NH, MODE, true>(a, st);
+            }
+        }
+    }
     if constexpr (MODE == MODE_FP8) {
         // stages of half the bytes: a deeper ring keeps as many bytes in flight
         if (DecSmem<D, 5, NH, true>::bytes(a.batch) <= kSmemLimit) return launch_decode<D, 5, NH, MODE>(a, st);
