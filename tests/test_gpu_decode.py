@@ -171,6 +171,43 @@ def test_large_batch_of_tiny_requests_matches_oracle():
     assert api.pa_get_error(ws) == 0
 
 
+@pytest.mark.parametrize("case", ["mixed_d128", "mixed_d64", "one_long_hkv1", "one_long_hkv1_capped"])
+def test_balanced_large_batch_plan_matches_oracle(case):
+    """Large batches (2 B Hkv above the SM count) take the balanced plan: equal
+    tile ranges per CTA over the (kv head, request) segments, a segment's
+    pieces merged by the second kernel.  Lengths 0, 1 and tile edges, a long
+    request cut into many pieces, and (capped) the fallback when a segment
+    would need more pieces than max_splits; twice, bit-identical."""
+    rng = np.random.default_rng({"mixed_d128": 31, "mixed_d64": 32, "one_long_hkv1": 33,
+                                 "one_long_hkv1_capped": 33}[case])
+    max_splits = 8 if case == "one_long_hkv1_capped" else MAX_SPLITS
+    if case.startswith("mixed"):
+        B, Hq, Hkv, D = (40, 32, 8, 128) if case == "mixed_d128" else (24, 16, 8, 64)
+        lens = [int(rng.choice([0, 1, 15, 16, 17, 129, 1000, 3000])) for _ in range(B)]
+        max_ctx = 3000
+    else:
+        B, Hq, Hkv, D = 200, 4, 1, 128
+        lens = [int(x) for x in rng.integers(1, 6, size=B)]
+        lens[77] = 8000
+        max_ctx = 8000
+    size = sum(-(-max(n, 1) // 16) * 16 for n in lens) + 64
+    st = W.make_decode_step(lens=lens, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D, n_layers=1, size=size,
+                            page_size=16, seed=int(rng.integers(1 << 30)), max_ctx=max_ctx, device="cuda")
+    # requests of length 0 have no new token: store the others' only
+    nz = torch.tensor([i for i, n in enumerate(lens) if n > 0], dtype=torch.long)
+    kb0, vb0 = bits(st.kv.k_buf), bits(st.kv.v_buf)
+    k_new, v_new, loc = st.k_new[nz].contiguous(), st.v_new[nz].contiguous(), st.loc[nz.to(st.loc.device)].contiguous()
+    api.pa_kv_store(st.kv.k_buf, st.kv.v_buf, 0, k_new, v_new, loc)
+    kb, vb = oracle.kv_store(kb0, vb0, 0, bits(k_new), bits(v_new), npy(loc))
+    ref = _oracle_full(st, kb, vb)
+    ws = _ws(B, Hq, Hkv, D, max_splits)
+    out1, _ = _decode(st, max_splits=max_splits, ws=ws)
+    assert_attention_close(npy(out1.float()), ref, f"balanced plan {case}")
+    out2, _ = _decode(st, max_splits=max_splits, ws=ws)
+    assert torch.equal(out1, out2)
+    assert api.pa_get_error(ws) == 0
+
+
 def test_bad_slot_sets_error_and_is_skipped():
     st = W.make_decode_step(lens=[40, 40], n_q_heads=8, n_kv_heads=2, head_dim=64, n_layers=1, size=256,
                             page_size=16, seed=8, device="cuda")
