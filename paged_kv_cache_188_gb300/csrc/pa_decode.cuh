@@ -117,7 +117,6 @@ struct DecodeArgs {
     int early_meta;      // launched behind another kernel: plan and page table before waiting for it
     int early_kv;        // ... and copy K/V tiles (not the requests' newest rows) before waiting for it
     int defer_merge;     // large batch: every split's partials written, merged by a second kernel (no tickets)
-    int plan_grid;       // CTAs of the decode launch (the plan the deferred merge recomputes)
     uint64_t wait_ns;    // time limit of the ring waits
     float scale_log2;
     // fused decode step (k_new != null): RoPE on q as it is loaded, and the new
@@ -1287,6 +1286,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
                 }
             }
         }
+        // deferred merge: the first split records the split count in the
+        // (otherwise unused) ticket word, which the merge kernel reads and zeroes
+        if constexpr (BAL) {
+            if (a.defer_merge && I.sb > 1 && I.s == 0 && tid == 0) a.counters[I.b * Hkv + I.h] = I.sb;
+        }
         if (I.sb > 1 && !a.defer_merge) {
             // ticket for (b, h): the barrier orders every thread's partial
             // stores before thread 0's acquire-release atomic (release: this
@@ -1318,10 +1322,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) paged_decode_kernel(const __gr
 // completed a (request, kv head) last would merge it, and the merges piled up
 // on the CTAs that were already behind.  This kernel merges every (request,
 // kv head) of more than one split, one per CTA at a time, over the whole GPU,
-// after the decode kernel (it waits for it first).  It recomputes the decode
-// launch's plan (plan_grid CTAs), so it sees the same split counts, and does
-// the in-kernel merge's arithmetic: split weights warp-parallel, each element
-// summed in split order.
+// after the decode kernel (it waits for it first).  Each (request, kv head)'s
+// split count is the one its first split recorded in the ticket word (the
+// kernel zeroes the word again), so no plan is recomputed here; the
+// arithmetic is the in-kernel merge's: split weights warp-parallel, each
+// element summed in split order.
 template <int D, int NH>
 __global__ void __launch_bounds__(kDecThreads) paged_decode_merge_kernel(const __grid_constant__ DecodeArgs a)
 {
@@ -1330,79 +1335,18 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_merge_kernel(const _
     constexpr int SPL = kDecMaxSplits / 32;   // splits per lane
     __shared__ float s_w[kDecMaxSplits * GMAX];   // [split][head] weights
     __shared__ float s_lt[GMAX];                  // weighted sums of l
-    __shared__ long long s_red[kDecWarps];
-    __shared__ int s_red2[kDecWarps], s_red3[kDecWarps];
-    __shared__ int s_tp[kDecMaxBatch + 1];        // balanced plan: each request's first tile
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.batch, Hkv = a.Hkv, G = a.G;
     pdl_wait();
     pdl_launch_dependents();
-    long long my_tot = 0;
-    int my_tiles = 0, my_tbmax = 0;
-    for (int b = tid; b < B; b += kDecThreads) {
-        const int n = clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
-        my_tot += n;
-        my_tiles += seg_tiles(n);
-        my_tbmax = max(my_tbmax, seg_tiles(n));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        my_tot += __shfl_xor_sync(0xffffffffu, my_tot, o);
-        my_tiles += __shfl_xor_sync(0xffffffffu, my_tiles, o);
-        my_tbmax = max(my_tbmax, __shfl_xor_sync(0xffffffffu, my_tbmax, o));
-    }
-    if (lane == 0) {
-        s_red[warp] = my_tot;
-        s_red2[warp] = my_tiles;
-        s_red3[warp] = my_tbmax;
-    }
-    __syncthreads();
-    long long tot = 0, tiles = 0;
-    int tb_max = 0;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
-        tot += s_red[w];
-        tiles += s_red2[w];
-        tb_max = max(tb_max, s_red3[w]);
-    }
-    // the decode launch's plan (this kernel runs only for deferred merges)
-    const DecPlan plan = make_plan(tot, B, Hkv, a.plan_grid, tiles, tb_max, a.max_splits, true);
-    if (plan.bal) {
-        // each request's first tile within a kv head's run: an exclusive prefix of its segment tiles
-        const int per = (B + kDecThreads - 1) / kDecThreads;
-        const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
-        int run = 0;
-        for (int b = b_lo; b < b_hi; ++b) run += seg_tiles(clamp_len(__ldg(a.seq_lens + b), a.max_ctx));
-        int incl = run;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        __syncthreads();   // s_red2 reuse
-        if (lane == 31) s_red2[warp] = incl;
-        __syncthreads();
-        int excl = incl - run;
-        for (int w = 0; w < warp; ++w) excl += s_red2[w];
-        for (int b = b_lo; b < b_hi; ++b) {
-            s_tp[b] = excl;
-            excl += seg_tiles(clamp_len(__ldg(a.seq_lens + b), a.max_ctx));
-        }
-        __syncthreads();
-    }
     const int64_t split_stride = (int64_t)a.cap_batch * a.Hq * D;
     const int64_t ml_stride = (int64_t)a.cap_batch * a.Hq * 2;
     for (int p = blockIdx.x; p < B * Hkv; p += gridDim.x) {
         const int b = p / Hkv, h = p - b * Hkv;
-        const int n = clamp_len(__ldg(a.seq_lens + b), a.max_ctx);
-        int sb, len;
-        if (plan.bal) {
-            const int tb = seg_tiles(n), S0 = h * (int)tiles + s_tp[b];
-            sb = (S0 + tb - 1) / plan.W - S0 / plan.W + 1;
-        } else {
-            split_of(n, plan, a.max_splits, sb, len);
-        }
-        if (sb <= 1) continue;   // written by the decode kernel
+        // the split count the decode kernel's first split recorded (0: one
+        // split, written by the decode kernel itself)
+        const int sb = __ldcg(a.counters + p);
+        if (sb <= 1 || sb > a.max_splits) continue;
         const int hq0 = h * G;
         for (int gg = warp; gg < G; gg += kDecWarps) {
             const float *ml = a.ml_part + ((int64_t)b * a.Hq + hq0 + gg) * 2;
@@ -1445,7 +1389,8 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_merge_kernel(const _
             const float lt = s_lt[gg];
             a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
         }
-        __syncthreads();   // s_w, s_lt reuse
+        __syncthreads();   // s_w, s_lt reuse; every thread has read the count
+        if (tid == 0) a.counters[p] = 0;
     }
 }
 
@@ -1602,8 +1547,7 @@ static pa_status dispatch_mode(const DecodeArgs &a0, int head_dim, cudaStream_t 
     if constexpr (MODE == MODE_PLAIN || MODE == MODE_FUSED || MODE == MODE_FP8) {
         // more (request, kv head) pairs than half the CTAs: many items per CTA,
         // merged by the second kernel
-        a.plan_grid = num_sms();
-        a.defer_merge = 2 * a.batch * a.Hkv > a.plan_grid;
+        a.defer_merge = 2 * a.batch * a.Hkv > num_sms();
     }
     if (head_dim == 128) return a.G > 8 ? dispatch_decode<128, 2, MODE>(a, st) : dispatch_decode<128, 1, MODE>(a, st);
     return a.G > 8 ? dispatch_decode<64, 2, MODE>(a, st) : dispatch_decode<64, 1, MODE>(a, st);
