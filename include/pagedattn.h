@@ -212,8 +212,11 @@ pa_status pa_rope_packed(void *q, int n_q_heads, void *k, int n_kv_heads, int he
  * (request, kv head) pairs as SMs, the merge runs inside the one decode
  * kernel (the CTA that completes a pair merges it).  A larger batch is two
  * kernels on `st`: decode, which writes every split's partials, then a merge
- * kernel spread over the whole GPU (it writes only out).  This also holds for
- * pa_decode_step and pa_paged_decode_attn_fp8.
+ * kernel spread over the whole GPU (it writes only out).  For such a batch
+ * every CTA takes an equal range of 16-token tiles over the (kv head,
+ * request) pairs, a pair's pieces being its splits (a pair that would need
+ * more than max_splits pieces falls back to splits of a common length).  This
+ * also holds for pa_decode_step and pa_paged_decode_attn_fp8.
  * Supported: head_dim in {64, 128}; 1 <= G <= 16; 1 <= max_splits <= 128;
  * batch <= 4096 and <= the workspace's cap_batch for these head counts and
  * max_splits.  A 16-token tile whose positions sit on one page moves as TMA
