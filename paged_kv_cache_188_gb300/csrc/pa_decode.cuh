@@ -1348,6 +1348,17 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_merge_kernel(const _
         const int sb = __ldcg(a.counters + p);
         if (sb <= 1 || sb > a.max_splits) continue;
         const int hq0 = h * G;
+        const float *obase = a.o_part + ((int64_t)b * a.Hq + hq0) * D;
+        // the first splits' partials of this thread's elements, requested
+        // before the (m, l) pairs (ordered loads: one round trip for both)
+        constexpr int SB = 8;
+        float v[EPT][SB];
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int e = tid + k * kDecThreads;
+#pragma unroll
+            for (int j = 0; j < SB; ++j) v[k][j] = ld_cg_ordered_if(e < G * D && j < sb, obase + e + j * split_stride);
+        }
         for (int gg = warp; gg < G; gg += kDecWarps) {
             const float *ml = a.ml_part + ((int64_t)b * a.Hq + hq0 + gg) * 2;
             float mv[SPL], lv[SPL];
@@ -1377,15 +1388,16 @@ __global__ void __launch_bounds__(kDecThreads) paged_decode_merge_kernel(const _
             if (lane == 0) s_lt[gg] = lt;
         }
         __syncthreads();
-        const float *obase = a.o_part + ((int64_t)b * a.Hq + hq0) * D;
 #pragma unroll
         for (int k = 0; k < EPT; ++k) {
             const int e = tid + k * kDecThreads;
             if (e >= G * D) continue;
             const int gg = e / D;
-            float acc = 0.f;
-#pragma unroll 8
-            for (int ss = 0; ss < sb; ++ss) acc += s_w[ss * G + gg] * __ldcg(obase + e + ss * split_stride);
+            float acc = 0.f;   // summed in split order
+#pragma unroll
+            for (int j = 0; j < SB; ++j)
+                if (j < sb) acc += s_w[j * G + gg] * v[k][j];
+            for (int ss = SB; ss < sb; ++ss) acc += s_w[ss * G + gg] * __ldcg(obase + e + ss * split_stride);
             const float lt = s_lt[gg];
             a.out[((int64_t)b * a.Hq + hq0) * D + e] = __float2bfloat16_rn(lt > 0.f ? acc / lt : 0.f);
         }
