@@ -53,3 +53,22 @@ def test_two_gloo_ranks_reduce_timing_and_bytes():
 def test_reference_arm_other_ranks_do_no_work():
     import bench
     assert bench.run_reference(None, 1, 2, 1) is None
+
+
+def test_reference_arm_line_on_the_host():
+    """Rank 0 of the reference arm times the float64 oracle on the host
+    cores: a bench line with the contract's keys, the oracle as its CPU
+    baseline, and no CUDA library loaded in the process."""
+    import types
+
+    import bench
+    from paged_kv_cache_188_gb300 import api
+    args = types.SimpleNamespace(steps=2, warmup=1)
+    line = bench.run_reference(args, 0, 1, 0)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["dtype"] == "f64" and line["steps"] == 2
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert api._lib is None
