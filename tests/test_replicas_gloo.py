@@ -57,18 +57,26 @@ def test_reference_arm_other_ranks_do_no_work():
 
 def test_reference_arm_line_on_the_host():
     """Rank 0 of the reference arm times the float64 oracle on the host
-    cores: a bench line with the contract's keys, the oracle as its CPU
-    baseline, and no CUDA library loaded in the process."""
-    import types
-
-    import bench
-    from paged_kv_cache_188_gb300 import api
-    args = types.SimpleNamespace(steps=2, warmup=1)
-    line = bench.run_reference(args, 0, 1, 0)
+    cores: a bench line with the contract's keys and the oracle as its CPU
+    baseline, from a process that never maps the CUDA library."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = (
+        "import json, sys, types\n"
+        "import bench\n"
+        "line = bench.run_reference(types.SimpleNamespace(steps=2, warmup=1), 0, 1, 0)\n"
+        "maps = open('/proc/self/maps').read()\n"
+        "print(json.dumps({'line': line, 'mapped': 'libpagedattn' in maps}))\n")
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    res = json.loads(out.stdout.strip().splitlines()[-1])
+    line = res["line"]
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
                 "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert key in line, key
     assert line["impl"] == "reference" and line["dtype"] == "f64" and line["steps"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
-    assert api._lib is None
+    assert not res["mapped"]
