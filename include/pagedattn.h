@@ -127,7 +127,9 @@ uint64_t pa_get_wait_timeout_ns(void);
  * A workspace is one caller-allocated device buffer, 256-byte aligned.  Its
  * first 4 bytes are the device error word.  Initialise it once with
  * pa_workspace_init before first use (it zeroes the error word and the decode
- * merge counters, which the decode kernel afterwards keeps at zero itself).
+ * merge counters, which the decode kernels afterwards return to zero
+ * themselves: the merge tickets, or for large batches the split counts that
+ * the merge kernel reads).
  *
  * Decode layout, derived only from (workspace_bytes, n_q_heads, n_kv_heads,
  * head_dim, max_splits), so changing the batch between calls moves nothing:
