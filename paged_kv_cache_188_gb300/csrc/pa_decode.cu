@@ -3,6 +3,15 @@
 // workspace, and pa_paged_decode_attn_noalloc with a fixed scratch array.
 #include "pa_decode.cuh"
 
+namespace pa {
+// Plain decode on prepared arguments, for the other translation units (the
+// cascade's no-group path): its kernel instances are compiled here only.
+pa_status decode_plain(const DecodeArgs &a, int head_dim, cudaStream_t st)
+{
+    return dispatch_mode<MODE_PLAIN>(a, head_dim, st);
+}
+}  // namespace pa
+
 using namespace pa;
 
 extern "C" pa_status pa_paged_decode_attn(const void *q, int batch, int n_q_heads, const void *k_buf,

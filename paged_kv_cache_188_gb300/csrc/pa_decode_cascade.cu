@@ -13,6 +13,10 @@
 // prefix row for the suffix launch, which plans only after waiting for it.
 #include "pa_decode.cuh"
 
+namespace pa {
+pa_status decode_plain(const DecodeArgs &a, int head_dim, cudaStream_t st);   // pa_decode.cu
+}
+
 using namespace pa;
 
 namespace pa {
@@ -93,7 +97,7 @@ extern "C" pa_status pa_paged_decode_attn_cascade(const void *q, int batch, int 
         if (!fill_decode_args(b, q, batch, n_q_heads, k_buf, v_buf, s, layer_id, req_to_token, req_rows, max_ctx,
                               req_pool_indices, seq_lens, scale, caps.max_splits, out, err, wb, w + L.b_off))
             return PA_ERR_CUDA;
-        return dispatch_mode<MODE_PLAIN>(b, s.head_dim, st);
+        return decode_plain(b, s.head_dim, st);
     }
     const DecodeWsLayout wa = decode_ws_layout(L.a_bytes, L.Hqv, s.n_kv_heads, s.head_dim, caps.max_splits);
     int32_t *req_start = reinterpret_cast<int32_t *>(w + L.start_off);
